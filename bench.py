@@ -1,0 +1,493 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = the whole hot path over one batch: the KV append of each
+sequence's new token (pa_reshape_and_cache) and paged decode attention over
+every sequence's history (pa_decode).  Workload: batch 256, 32 q / 8 kv heads,
+head_dim 128, bf16, block size 16, context lengths lognormal (median 800,
+sigma 0.5) clipped to [16, 4096], pool 1.2x the blocks needed.
+
+Prints one JSON line (rank 0):
+  value      algorithmic GB/s of a step with inputs resident in HBM
+             (KV read + Q read + O write of decode, plus the append's
+             read + write), timed with CUDA events over exactly K steps
+  e2e        the same metric through the C ABI from pinned host buffers: per
+             step the host allocator reserves the slots, tables/lens/q/new
+             K,V go host->device, the kernels run, the output comes back
+  roofline   pa_decode's algorithmic bytes / its mean CUDA-event duration,
+             against the measured HBM copy bandwidth
+  cpu_baseline  the fp64 oracle on a bounded sample, on the host
+
+``--impl reference`` times the oracle instead (the reference arm).
+Multi-GPU: independent replicas, one per rank (the path needs no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_142_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-steps/s at batch 256"
+UNIT = "GB/s"
+WORKLOAD = ("paged decode step (KV append + decode), batch 256, 32 q / 8 kv heads, head_dim 128, "
+            "bf16, block 16, lens lognormal(median 800, sigma 0.5) clipped [16,4096], "
+            "pool 1.2x needed, values N(0,1)*0.5")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_gqa_bf16_b256.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_142_gb300", "csrc", f)
+                  for f in ("decode_kernel.cuh", "decode.cuh", "ptx.cuh")]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per pa_decode launch from the committed ncu summary, if it
+    was taken on the current kernel source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    kv = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+    if kv.get("kernel_source_hash") != kernel_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for t, r in self.rows if any(a - 0.05 <= t <= b + 0.05 for a, b in self.windows)]
+        used = inside or [min(self.rows, key=lambda tr: min(abs(tr[0] - a) for a, _ in self.windows))[1]]
+        sm = [float(r[1]) for r in used if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in used if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in used for k in range(4) if len(r) > 5 + k and r[5 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# --------------------------------------------------------------------------
+# byte accounting (algorithmic, per step)
+# --------------------------------------------------------------------------
+def step_bytes(lens: np.ndarray, B, H, Hkv, D, e, e_out):
+    kv = int(lens.sum()) * 2 * Hkv * D * e       # every visible token's K and V, each kv head
+    qo = B * H * D * e + B * H * D * e_out        # queries in, outputs out
+    append = 2 * (2 * B * Hkv * D * e) + 8 * B    # new K,V read + written, slot ids
+    return kv + qo, append
+
+
+# --------------------------------------------------------------------------
+# reference arm / CPU baseline: the fp64 oracle on a bounded sample
+# --------------------------------------------------------------------------
+def _oracle_sample_setup(wl, nseq):
+    import oracle
+    st = wl.seq_starts
+    a = oracle.OracleAllocator(wl.num_blocks, wl.block_size, wl.free_order)
+    per = [a.append_tokens(a.seq_create(), int(n)) for n in wl.context_lens]
+    tables = np.zeros((wl.num_seqs, wl.max_blocks_per_seq), dtype=np.int64)
+    for i in range(wl.num_seqs):
+        t = a.block_table(i)
+        tables[i, :len(t)] = t
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    kc = np.zeros(shape, dtype=np.float64)
+    vc = np.zeros(shape, dtype=np.float64)
+    for i in range(nseq):
+        oracle.reshape_and_cache(wl.key_hist.f32[st[i]:st[i + 1]], wl.value_hist.f32[st[i]:st[i + 1]],
+                                 kc, vc, per[i])
+    return tables, kc, vc
+
+
+def _oracle_child(argv):
+    """Runs in a child process with one BLAS thread: time the oracle decoding
+    sequences 0..nseq-1 in turn, either ``steps`` decodes or for ``budget`` s."""
+    budget, nseq, steps = float(argv[0]), int(argv[1]), int(argv[2])
+    import oracle
+    wl = W.gqa_bf16()
+    tables, kc, vc = _oracle_sample_setup(wl, nseq)
+    e = W.elem_bytes(wl.dtype)
+    per_seq = [step_bytes(wl.context_lens[i:i + 1], 1, wl.num_q_heads, wl.num_kv_heads,
+                          wl.head_dim, e, e)[0] for i in range(nseq)]
+    times, nbytes = [], []
+    t_start = time.perf_counter()
+    k = 0
+    while True:
+        i = k % nseq
+        t0 = time.perf_counter()
+        oracle.paged_decode(wl.q.f32, kc, vc, tables, wl.context_lens, wl.scale, wl.num_kv_heads,
+                            seqs=[i])
+        times.append(time.perf_counter() - t0)
+        nbytes.append(per_seq[i])
+        k += 1
+        if (steps and k >= steps) or (not steps and time.perf_counter() - t_start >= budget):
+            break
+    print(json.dumps({"times": times, "bytes": nbytes}))
+
+
+def run_oracle(budget_s: float, nseq: int, steps: int = 0):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle_child",
+                        str(budget_s), str(nseq), str(steps)],
+                       capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle baseline failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args):
+    """The oracle as the reference arm: each step decodes a bounded sample of
+    the workload's sequences, sized so the K + W steps take about two minutes."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cal = run_oracle(0, 4, steps=4)
+    t_seq = max(1e-4, sum(cal["times"]) / len(cal["times"]))
+    per_step = max(1, min(256, int(120.0 / max(1, args.steps + args.warmup) / t_seq)))
+    res = run_oracle(0, per_step, steps=per_step * (args.steps + args.warmup))
+    times = res["times"][per_step * args.warmup:]
+    nbytes = res["bytes"][per_step * args.warmup:]
+    t = sum(times)
+    value = sum(nbytes) / t / 1e9
+    sample = (f"fp64 oracle decode of {per_step} of the 256 sequences per step "
+              f"(single process, 1 BLAS thread)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "num_seqs": 256, "sample_seqs_per_step": per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "seq_steps_per_s": round(per_step * args.steps / t, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_cache_142_gb300 import build as B_
+    B_.build(quiet=True)
+    from paged_kv_cache_142_gb300 import ops
+
+    wl = W.gqa_bf16()
+    B, H, Hkv, D, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    e = W.elem_bytes(wl.dtype)
+    K, Wm = args.steps, args.warmup
+    # pool: the workload's 1.2x plus room for the e2e leg's growth
+    grow = K + Wm + 1
+    NB = wl.num_blocks + B * (grow // bs + 2)
+    free_order = np.concatenate([wl.free_order, np.arange(wl.num_blocks, NB, dtype=np.int32)])
+    alloc = ops.BlockAllocator(NB, bs, free_order)
+    seqs = [alloc.seq_create() for _ in range(B)]
+    hist = [alloc.append_tokens(s, int(n)) for s, n in zip(seqs, wl.context_lens)]
+    slots_all = np.concatenate(hist)
+    new_slots = np.array([h[-1] for h in hist], dtype=np.int64)  # this step's token
+    max_len = int(wl.context_lens.max())
+    e2e_max_len = max_len + grow
+    maxb = -(-e2e_max_len // bs)
+    tables, lens = alloc.export_tables(seqs, maxb)
+
+    kc = torch.zeros((NB, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+
+    def dev_vals(v):
+        return torch.from_numpy(np.ascontiguousarray(v.bits)).view(torch.bfloat16).to(dev)
+
+    key_all, val_all = dev_vals(wl.key_hist), dev_vals(wl.value_hist)
+    ops.pa_reshape_and_cache(key_all, val_all, torch.from_numpy(slots_all).to(dev), kc, vc)
+    st = wl.seq_starts
+    last = torch.from_numpy(st[1:] - 1).to(dev)
+    new_k = key_all.index_select(0, last).contiguous()
+    new_v = val_all.index_select(0, last).contiguous()
+    del key_all, val_all
+    q = dev_vals(wl.q)
+    t_tables = torch.from_numpy(tables).to(dev)
+    t_lens = torch.from_numpy(lens).to(dev)
+    t_slots = torch.from_numpy(new_slots).to(dev)
+    out = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+    ws = ops.make_workspace(B, H, Hkv, D, bs, "bf16", e2e_max_len, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    decode_bytes, append_bytes = step_bytes(lens, B, H, Hkv, D, e, 2)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+
+    def step():
+        ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
+        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws)
+
+    # ---------------- device-resident steps ----------------
+    for _ in range(Wm):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    t0e.record(stream)
+    for k in range(K):
+        ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
+        ev[k][0].record(stream)
+        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws)
+        ev[k][1].record(stream)
+    t1e.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    sampler.mark(w0, w1)
+    if world > 1:
+        dist.barrier()
+    total_ms = t0e.elapsed_time(t1e)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    dev_status = ops.pa_workspace_error(ws)
+    if dev_status != 0:
+        raise RuntimeError(f"device status {dev_status} after the timed steps")
+
+    # ---------------- end to end through the C ABI, host buffers ----------------
+    pin = dict(pin_memory=True)
+    h_q = torch.from_numpy(np.ascontiguousarray(wl.q.bits)).view(torch.bfloat16).pin_memory()
+    h_k = new_k.cpu().pin_memory()
+    h_v = new_v.cpu().pin_memory()
+    h_slots = torch.empty(B, dtype=torch.int64, **pin)
+    h_tables = torch.empty((B, maxb), dtype=torch.int32, **pin)
+    h_lens = torch.empty(B, dtype=torch.int32, **pin)
+    h_out = torch.empty((B, H, D), dtype=torch.bfloat16, **pin)
+    d_q = torch.empty_like(q)
+    d_k = torch.empty_like(new_k)
+    d_v = torch.empty_like(new_v)
+    d_slots = torch.empty_like(t_slots)
+    d_tables = torch.empty_like(t_tables)
+    d_lens = torch.empty_like(t_lens)
+    d_pairs = torch.empty((B, 2), dtype=torch.int64, device=dev)
+    # the device-timed steps rewrote the last token in place; the e2e leg
+    # appends new tokens after it
+    e2e_bytes = []
+    n_cow = 0
+
+    def e2e_step():
+        nonlocal n_cow
+        slots, pairs = alloc.append_slots(seqs)        # host allocator: reserve slots
+        tb, ln = alloc.export_tables(seqs, maxb)
+        h_slots.numpy()[:] = slots
+        h_tables.numpy()[:] = tb
+        h_lens.numpy()[:] = ln
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_tables.copy_(h_tables, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        if len(pairs):
+            d_pairs[:len(pairs)].copy_(torch.from_numpy(pairs))
+            ops.pa_copy_blocks(kc, vc, d_pairs[:len(pairs)])
+            n_cow += len(pairs)
+        ops.pa_reshape_and_cache(d_k, d_v, d_slots, kc, vc)
+        ops.pa_decode(d_out, d_q, kc, vc, d_tables, d_lens, wl.scale, Hkv, e2e_max_len, ws)
+        h_out.copy_(d_out, non_blocking=True)
+        return ln
+
+    d_out = torch.empty_like(out)
+    for _ in range(min(Wm, 3)):
+        ln = e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w2 = time.time()
+    e0.record(stream)
+    for _ in range(K):
+        ln = e2e_step()
+        e2e_bytes.append(sum(step_bytes(ln, B, H, Hkv, D, e, 2)))
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    w3 = time.time()
+    sampler.mark(w2, w3)
+    e2e_ms = e0.elapsed_time(e1)
+    sampler.stop()
+    if ops.pa_workspace_error(ws) != 0:
+        raise RuntimeError("device status after the e2e steps")
+
+    h2d = (h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_slots.numel() * 8
+           + h_tables.numel() * 4 + h_lens.numel() * 4)
+    d2h = h_out.numel() * 2
+
+    # max over ranks
+    t_step = total_ms / K
+    t_dec = statistics.mean(dec_ms)
+    t_e2e = e2e_ms / K
+    vals = [t_step, t_dec, t_e2e]
+    if world > 1:
+        tt = torch.tensor(vals, dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        vals = tt.tolist()
+        t_step, t_dec, t_e2e = vals
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    step_b = decode_bytes + append_bytes
+    value = world * step_b / (t_step * 1e-3) / 1e9
+    achieved = decode_bytes / (t_dec * 1e-3) / 1e9
+    e2e_val = world * statistics.mean(e2e_bytes) / (t_e2e * 1e-3) / 1e9
+    pt, ctas = ops.pa_decode_plan(B, H, Hkv, D, bs, "bf16", e2e_max_len)
+    clocks = sampler.summary()
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        res = run_oracle(args.cpu_seconds, 64)
+        tot = sum(res["times"])
+        cpu = {"value": round(sum(res["bytes"]) / tot / 1e9, 4), "unit": UNIT, "cores": 1,
+               "kind": "oracle",
+               "sample": (f"fp64 oracle decode of the first 64 of the 256 sequences in turn for "
+                          f"{tot:.1f} s ({len(res['times'])} sequence decodes, "
+                          f"{len(res['times']) / tot:.1f} seq-steps/s), 1 process, 1 BLAS thread")}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(t_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "num_seqs": B, "num_q_heads": H, "num_kv_heads": Hkv,
+                   "head_dim": D, "block_size": bs, "total_tokens": int(lens.sum()),
+                   "max_context_len": max_len, "partition_tokens": pt, "ctas": ctas,
+                   "l2": "inputs larger than L2: %.2f GB of KV read per step vs 129 MB L2"
+                         % (decode_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "seq_steps_per_s": round(world * B / (t_step * 1e-3), 1),
+        "decode_ms": round(t_dec, 5),
+        "decode_bytes_per_step": decode_bytes,
+        "append_bytes_per_step": append_bytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(), "kernel": "pa_decode",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "pct_of_nominal_8tbs": round(100 * achieved / 8000.0, 2),
+        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "seq_steps_per_s": round(world * B / (t_e2e * 1e-3), 1),
+                "ms_per_step": round(t_e2e, 5)},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--_oracle_child":
+        _oracle_child(sys.argv[2:])
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * pa.h -- C ABI of the GB300 paged KV cache library (libpa_gb300.so).
+ *
+ * The operations follow the three pages on PagedAttention, cited by title
+ * and section:
+ *   [vLLM2] "vLLM internals (2) - why PagedAttention splits the KV cache into
+ *           pages" (youngju.dev): block table, block size, sharing.
+ *   [PA]    "PagedAttention" (icarus.shaojiemike.top): "Block Table 如何工作",
+ *           "KV Cache 为什么难管理", "支持块级共享", "不改变模型精度".
+ *   [KV02]  "LLM KV cache 02 - serving engine KV" (ttlab.hopto.org), section 2:
+ *           blocks, block table, sharing, copy-on-write.
+ *
+ * Conventions shared by every call:
+ *   - KV cache layout (the pages name none; this library fixes it): k_cache
+ *     and v_cache are each a row-major array [num_blocks][num_kv_heads]
+ *     [block_size][head_dim] of `dtype`.  One (block, kv head) tile of K is
+ *     block_size*head_dim contiguous elements; one whole block across kv heads
+ *     is contiguous too.  Both base pointers must be 16-byte aligned.
+ *   - Every pointer named "device" is a CUDA device pointer owned by the
+ *     caller; the library never allocates, frees or keeps device memory.
+ *     "host" pointers are read or written before the call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
+ *     work is enqueued asynchronously on it; the call does not synchronise.
+ *   - Argument errors are detected on the host and returned before anything is
+ *     enqueued.  A launch failure returns PA_ERR_CUDA.  No call throws,
+ *     prints, exits or traps.
+ *   - Supported: dtype F32 or BF16; head_dim 64, 128 or 256; block_size a
+ *     power of two from 1 to 256; num_q_heads / num_kv_heads in {1,2,4,8}.
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* a size, pointer or precondition is wrong       */
+  PA_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shapes          */
+  PA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed            */
+  PA_ERR_OOM = 4,           /* allocator: no free block (state unchanged)      */
+  PA_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required      */
+  PA_ERR_DEVICE_TIMEOUT = 6 /* a bounded device wait gave up (see pa_decode)   */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_DTYPE_F32 = 0,
+  PA_DTYPE_BF16 = 1
+} pa_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_string(pa_status status);
+
+/* Library version string, e.g. "pa_gb300 1.0 sm_103a". */
+const char* pa_version(void);
+
+/* ------------------------------------------------------------------------
+ * KV append -- [PA] "Block Table 如何工作": a generating sequence writes the new
+ * token's K/V into the current block; [KV02] section 2: a new block is taken
+ * when the current one is full.  Slot = physical_block * block_size + offset.
+ *
+ * For t < num_tokens with s = slot_mapping[t] >= 0, writes
+ *   k_cache[s / block_size][h][s % block_size][:] = key[t][h][:]
+ *   v_cache[...same...]                             = value[t][h][:]
+ * for every kv head h.  Negative slots (padding) are skipped; slots >=
+ * num_blocks*block_size are skipped too (never written).
+ *
+ *   key, value    device, [num_tokens][num_kv_heads][head_dim] of dtype
+ *   slot_mapping  device, int64 [num_tokens]
+ *   k_cache/v_cache device, layout above
+ * Two tokens mapped to the same slot in one call race (last writer wins).
+ * num_tokens == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
+                               const int64_t* slot_mapping,
+                               void* k_cache, void* v_cache,
+                               int32_t num_blocks, int32_t block_size,
+                               int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
+ * Copy-on-write block copy -- [PA] "支持块级共享"; [KV02] section 2: a
+ * shared block is copied to a fresh one only when a branch has to write
+ * different content into it.
+ *
+ * For each pair j: k_cache[dst_j] = k_cache[src_j] and v_cache[dst_j] =
+ * v_cache[src_j] (all kv heads, all block_size tokens), where
+ * block_pairs[2j] = src_j and block_pairs[2j+1] = dst_j.
+ *   block_pairs   device, int64 [num_pairs][2]
+ * Precondition (not checked on the device): destinations are distinct and
+ * none is also a source in the same call; then the result equals copying
+ * from the state before the call.  Pairs naming a block outside
+ * [0, num_blocks) are skipped.  num_pairs == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache,
+                         int32_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                         const int64_t* block_pairs, int32_t num_pairs,
+                         void* stream);
+
+/* ------------------------------------------------------------------------
+ * Paged decode attention -- [PA] "Block Table 如何工作": the kernel reads the
+ * block table to turn logical block numbers into physical block ids, so each
+ * sequence sees its K/V in token order; [PA] "不改变模型精度": the result is
+ * the attention over the contiguous history.
+ *
+ * For sequence i < num_seqs, query head h, kv head g = h / (num_q_heads /
+ * num_kv_heads) and len = context_lens[i] (the token appended this step
+ * included):
+ *   K_t = k_cache[block_tables[i*max_blocks_per_seq + t/block_size]][g][t%block_size]
+ *   out[i][h][:] = sum_t softmax_t(scale * q[i][h]·K_t) * V_t ,  t < len
+ * and out[i][h][:] = 0 when len == 0.  Accumulation is fp32.
+ *
+ *   out           device, [num_seqs][num_q_heads][head_dim] of out_dtype
+ *   q             device, [num_seqs][num_q_heads][head_dim] of dtype
+ *   block_tables  device, int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(len/block_size) are never read; every entry read must
+ *                 be in [0, num_blocks)
+ *   context_lens  device, int32 [num_seqs]; each in [0, max_context_len]
+ *   max_context_len  host bound used for planning (no device sync)
+ *   partition_tokens 0 = automatic; else the number of tokens each split-K
+ *                 partition covers (rounded up to the plan's granularity)
+ *   workspace     device scratch of at least pa_decode_workspace_size(...)
+ *                 bytes, 256-byte aligned, ZERO-FILLED before its first use
+ *                 (e.g. pa_workspace_init).  Every call leaves its
+ *                 bookkeeping words zero again, so one workspace serves any
+ *                 number of calls issued in stream order; calls that overlap
+ *                 on the GPU must use different workspaces.
+ * A long history is split into partitions processed by different CTAs; each
+ * writes (max, sum, unnormalised output) to the workspace and the last CTA
+ * to finish a (sequence, kv head) merges them by log-sum-exp.
+ * If a bounded device wait ever expires, the kernel stops early, the output
+ * is undefined, and pa_workspace_error() reports PA_ERR_DEVICE_TIMEOUT.
+ * ---------------------------------------------------------------------- */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, pa_dtype dtype,
+                                int32_t max_context_len, int32_t partition_tokens);
+
+pa_status pa_decode(void* out, pa_dtype out_dtype,
+                    const void* q, int32_t num_seqs, int32_t num_q_heads,
+                    const void* k_cache, const void* v_cache,
+                    int32_t num_blocks, int32_t block_size,
+                    int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t max_context_len,
+                    float scale, int32_t partition_tokens,
+                    void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* Partition size and CTA count pa_decode would use (host only; either out
+ * pointer may be NULL). */
+pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, pa_dtype dtype,
+                         int32_t max_context_len, int32_t partition_tokens,
+                         int32_t* partition_tokens_out, int32_t* num_ctas_out);
+
+/* Zero a decode workspace (enqueued on `stream`). */
+pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then reads the workspace's device error word into
+ * *device_status (PA_OK or PA_ERR_DEVICE_TIMEOUT) and clears it. */
+pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_status);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator -- [vLLM2] block-table section and [KV02] section 2:
+ * fixed-size blocks handed out on demand from anywhere in the pool; [PA]
+ * "Block Table 如何工作": full blocks trigger a new allocation, freed blocks
+ * nobody references return to the pool; [PA] "支持块级共享": reference
+ * counts, fork and copy-on-write.  Host memory only; not thread-safe (one
+ * caller at a time per handle).
+ *
+ * Policy: the free list starts in `free_order` (a permutation of
+ * 0..num_blocks-1; NULL = identity); allocation takes the front; a block
+ * whose count drops to 0 goes to the back.  Sequence ids count up from 0
+ * and are never reused.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_allocator pa_allocator;
+
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                          pa_allocator** out);
+void      pa_alloc_destroy(pa_allocator* a);
+int32_t   pa_alloc_num_blocks(const pa_allocator* a);
+int32_t   pa_alloc_block_size(const pa_allocator* a);
+int32_t   pa_alloc_num_free(const pa_allocator* a);
+/* Reference count of `block` (-1 if out of range). */
+int32_t   pa_alloc_refcount(const pa_allocator* a, int32_t block);
+/* Take one block (count 1) -> *block; PA_ERR_OOM if none is free. */
+pa_status pa_alloc_allocate(pa_allocator* a, int32_t* block);
+pa_status pa_alloc_incref(pa_allocator* a, int32_t block);
+/* Drop one reference; at zero the block goes to the back of the free list.
+ * PA_ERR_INVALID_ARG if the block is already free. */
+pa_status pa_alloc_decref(pa_allocator* a, int32_t block);
+
+/* New empty sequence -> *seq. */
+pa_status pa_alloc_seq_create(pa_allocator* a, int32_t* seq);
+/* New sequence sharing every block of `parent` (each count + 1). */
+pa_status pa_alloc_fork(pa_allocator* a, int32_t parent, int32_t* child);
+/* Reserve the slot of the next token of `seq`.  With pos = current length:
+ * pos % block_size == 0 -> a fresh block is appended to the table; else if
+ * the last block is shared (count > 1) it is replaced by a new block and
+ * (old, new) is reported in *cow_src, *cow_dst (both -1 otherwise).
+ * *slot = table[pos/bs]*bs + pos%bs.  PA_ERR_OOM leaves the state unchanged. */
+pa_status pa_alloc_append_slot(pa_allocator* a, int32_t seq, int64_t* slot,
+                               int32_t* cow_src, int32_t* cow_dst);
+/* One append_slot per entry of seqs[0..n), in order.  slots[j] receives
+ * sequence seqs[j]'s slot; copy pairs are appended to cow_pairs ([n][2],
+ * int64) and counted in *num_cow.  Stops at the first failure; *num_done
+ * tells how many appends took effect. */
+pa_status pa_alloc_append_slots(pa_allocator* a, const int32_t* seqs, int32_t n,
+                                int64_t* slots, int64_t* cow_pairs, int32_t* num_cow,
+                                int32_t* num_done);
+/* n successive append_slot calls on an unshared sequence (bulk prompt
+ * fill); slots[0..n) receive the slots.  PA_ERR_INVALID_ARG if a copy would
+ * be needed.  On PA_ERR_OOM nothing changes. */
+pa_status pa_alloc_append_tokens(pa_allocator* a, int32_t seq, int32_t n, int64_t* slots);
+/* Release every block of `seq` in table order; the id becomes invalid. */
+pa_status pa_alloc_free_seq(pa_allocator* a, int32_t seq);
+/* Length of `seq` (-1 if it is not live). */
+int32_t   pa_alloc_seq_len(const pa_allocator* a, int32_t seq);
+/* Number of sequences currently live. */
+int32_t   pa_alloc_num_seqs(const pa_allocator* a);
+/* Copy the block table of `seq` into out[0..cap); *n = its length. */
+pa_status pa_alloc_block_table(const pa_allocator* a, int32_t seq, int32_t* out, int32_t cap,
+                               int32_t* n);
+/* Dense tables for a batch: tables[j*max_blocks + k] = block k of seqs[j]
+ * (pad_value past its end), lens[j] = its length.  PA_ERR_INVALID_ARG if a
+ * table does not fit in max_blocks. */
+pa_status pa_alloc_export_tables(const pa_allocator* a, const int32_t* seqs, int32_t n,
+                                 int32_t* tables, int32_t max_blocks, int32_t* lens,
+                                 int32_t pad_value);
+/* Copy the free list, front first, into out[0..cap); *n = its length. */
+pa_status pa_alloc_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
+/* Copy the live sequence ids, ascending, into out[0..cap); *n = count. */
+pa_status pa_alloc_live_seqs(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_GB300_H */

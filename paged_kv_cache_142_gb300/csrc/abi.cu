@@ -1,0 +1,322 @@
+// C ABI shim: argument validation, split-K planning, workspace carve-up and
+// launches on the caller's stream.  Declarations and contracts: include/pa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "decode.cuh"
+#include "pa.h"
+
+namespace pa {
+bool decode_info_bf16(int head_dim, int group, DecodeKernelInfo* info);
+bool decode_info_f32(int head_dim, int group, DecodeKernelInfo* info);
+
+bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInfo* info) {
+  return dtype_bf16 ? decode_info_bf16(head_dim, group, info)
+                    : decode_info_f32(head_dim, group, info);
+}
+}  // namespace pa
+
+namespace {
+
+using pa::DecodeKernelInfo;
+using pa::DecodeParams;
+
+constexpr int kMaxSmem = 227 * 1024;
+constexpr int kDefaultPartTokens = 256;
+
+int dtype_bytes(pa_dtype d) {
+  return d == PA_DTYPE_F32 ? 4 : (d == PA_DTYPE_BF16 ? 2 : 0);
+}
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                            int32_t head_dim, pa_dtype dtype) {
+  if (num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0) return PA_ERR_INVALID_ARG;
+  if (dtype_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
+  if (!is_pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
+  const int64_t row = static_cast<int64_t>(head_dim) * dtype_bytes(dtype);
+  if (row % 16 != 0) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+struct Plan {
+  DecodeKernelInfo info;
+  int group;
+  int part_tokens;
+  int max_parts;
+  int smem;
+  int off_sc, off_red, off_tbl, off_prefix, off_bar;
+  size_t ws_counters, ws_ml, ws_o, ws_total;
+};
+
+pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t block_size, pa_dtype dtype,
+                    int32_t max_context_len, int32_t partition_tokens, Plan* pl) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+      partition_tokens < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (dtype_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
+  if (!is_pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  if (!pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
+    return PA_ERR_UNSUPPORTED;
+  pl->group = G;
+  // partition size: a multiple of the block size and of the stage; at most
+  // part/2 partitions per sequence (the merge stages 2 floats per partition
+  // and head in the score buffer)
+  const int64_t gran = block_size > pl->info.tokens_per_stage ? block_size : pl->info.tokens_per_stage;
+  int64_t pt = round_up(partition_tokens > 0 ? partition_tokens : kDefaultPartTokens, gran);
+  while (ceil_div(max_context_len, pt) > pt / 2) pt *= 2;
+  if (pt > (1 << 20)) return PA_ERR_UNSUPPORTED;
+  pl->part_tokens = static_cast<int>(pt);
+  pl->max_parts = static_cast<int>(ceil_div(max_context_len, pt) > 1 ? ceil_div(max_context_len, pt) : 1);
+  // shared memory
+  int64_t off = pl->info.ring_bytes;
+  pl->off_sc = static_cast<int>(off);
+  off += round_up(pt * G * 4, 16);
+  pl->off_red = static_cast<int>(off);
+  off += round_up((static_cast<int64_t>(pa::kConsumerWarps) * G * head_dim + 2 * pa::kConsumerWarps * G + 2 * G) * 4, 16);
+  pl->off_tbl = static_cast<int>(off);
+  off += round_up((pt / block_size + 1) * 4, 16);
+  pl->off_prefix = static_cast<int>(off);
+  off += round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
+  pl->off_bar = static_cast<int>(off);
+  off += 2 * pa::kStages * 8;
+  if (off + 64 > kMaxSmem) return PA_ERR_UNSUPPORTED;  // + static shared memory
+  pl->smem = static_cast<int>(off);
+  // workspace: header | counters | (max, sum) partials | output partials
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  pl->ws_counters = 256;
+  int64_t w = 256 + round_up(rows * 4, 256);
+  pl->ws_ml = static_cast<size_t>(w);
+  if (pl->max_parts > 1) {
+    w += round_up(rows * pl->max_parts * G * 2 * 4, 256);
+    pl->ws_o = static_cast<size_t>(w);
+    w += round_up(rows * pl->max_parts * G * static_cast<int64_t>(head_dim) * 4, 256);
+  } else {
+    pl->ws_o = static_cast<size_t>(w);
+  }
+  pl->ws_total = static_cast<size_t>(w);
+  return PA_OK;
+}
+
+// Per-kernel dynamic shared memory attribute and occupancy, cached.
+struct KernelCache {
+  const void* fn;
+  int device;
+  int smem_set;
+  int smem_occ;
+  int occ;
+};
+std::mutex g_mu;
+KernelCache g_cache[64];
+int g_ncache = 0;
+
+pa_status prepare_kernel(const void* fn, int smem, int* ctas) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  KernelCache* kc = nullptr;
+  for (int i = 0; i < g_ncache; ++i)
+    if (g_cache[i].fn == fn && g_cache[i].device == dev) kc = &g_cache[i];
+  if (!kc) {
+    if (g_ncache == 64) return PA_ERR_UNSUPPORTED;
+    kc = &g_cache[g_ncache++];
+    *kc = KernelCache{fn, dev, 0, -1, 0};
+  }
+  if (smem > kc->smem_set) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    kc->smem_set = smem;
+  }
+  if (kc->smem_occ != smem) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, pa::kDecodeThreads, smem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    kc->occ = occ;
+    kc->smem_occ = smem;
+  }
+  if (kc->occ <= 0) return PA_ERR_UNSUPPORTED;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PA_ERR_CUDA;
+  *ctas = sms * kc->occ;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OOM: return "PA_ERR_OOM";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+const char* pa_version(void) { return "pa_gb300 1.0 sm_103a"; }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, pa_dtype dtype, void* stream) {
+  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int32_t row = head_dim * dtype_bytes(dtype);
+  cudaError_t e = pa::launch_reshape_and_cache(key, value, num_tokens, slot_mapping, k_cache,
+                                               v_cache, num_blocks, block_size, num_kv_heads, row,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                         const int64_t* block_pairs, int32_t num_pairs, void* stream) {
+  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  const int64_t block_bytes =
+      static_cast<int64_t>(num_kv_heads) * block_size * head_dim * dtype_bytes(dtype);
+  cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, num_blocks, block_bytes, block_pairs,
+                                         num_pairs, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, pa_dtype dtype,
+                                int32_t max_context_len, int32_t partition_tokens) {
+  Plan pl;
+  if (make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype, max_context_len,
+                partition_tokens, &pl) != PA_OK)
+    return 0;
+  return pl.ws_total;
+}
+
+pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, pa_dtype dtype,
+                         int32_t max_context_len, int32_t partition_tokens,
+                         int32_t* partition_tokens_out, int32_t* num_ctas_out) {
+  Plan pl;
+  pa_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                           max_context_len, partition_tokens, &pl);
+  if (st != PA_OK) return st;
+  if (partition_tokens_out) *partition_tokens_out = pl.part_tokens;
+  if (num_ctas_out) {
+    int ctas = 0;
+    st = prepare_kernel(pl.info.fn, pl.smem, &ctas);
+    if (st != PA_OK) return st;
+    *num_ctas_out = ctas;
+  }
+  return PA_OK;
+}
+
+pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_seqs,
+                    int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                    int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                    int32_t head_dim, pa_dtype dtype, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t max_context_len, float scale, int32_t partition_tokens,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (dtype_bytes(out_dtype) == 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_context_len)
+    return PA_ERR_INVALID_ARG;
+  Plan pl;
+  st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype, max_context_len,
+                 partition_tokens, &pl);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < pl.ws_total || !aligned16(workspace))
+    return PA_ERR_WORKSPACE;
+  int ctas = 0;
+  st = prepare_kernel(pl.info.fn, pl.smem, &ctas);
+  if (st != PA_OK) return st;
+  const int64_t max_items = static_cast<int64_t>(num_seqs) * num_kv_heads * pl.max_parts;
+  if (ctas > max_items) ctas = static_cast<int>(max_items);
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_context_len = max_context_len;
+  p.part_tokens = pl.part_tokens;
+  p.max_parts = pl.max_parts;
+  p.out_bf16 = out_dtype == PA_DTYPE_BF16 ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.off_sc = pl.off_sc;
+  p.off_red = pl.off_red;
+  p.off_tbl = pl.off_tbl;
+  p.off_prefix = pl.off_prefix;
+  p.off_bar = pl.off_bar;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.ws_err = reinterpret_cast<int32_t*>(ws);
+  p.ws_counters = reinterpret_cast<int32_t*>(ws + pl.ws_counters);
+  p.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
+  p.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
+
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(pl.info.fn, dim3(static_cast<unsigned>(ctas)),
+                                   dim3(pa::kDecodeThreads), args, static_cast<size_t>(pl.smem),
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes == 0) return PA_OK;
+  return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_status) {
+  if (!workspace || !device_status) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(v), s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  *device_status = v;
+  return PA_OK;
+}
+
+}  // extern "C"

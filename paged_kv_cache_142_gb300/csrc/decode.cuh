@@ -1,0 +1,72 @@
+// Internal interface between the C ABI shim and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kDecodeThreads = 32 + kConsumerThreads;  // warp 0 streams, warps 1-4 compute
+constexpr int kStageBytes = 8192;                      // K or V rows per ring stage
+constexpr int kStages = 6;                             // ring depth
+constexpr uint64_t kWaitLimitNs = 2000000000ull;       // bounded device waits: 2 s
+
+// Device error codes written to the workspace header (match pa_status).
+constexpr int kDevErrInvalidArg = 1;
+constexpr int kDevErrTimeout = 6;
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t max_blocks_per_seq;
+  int32_t max_context_len;
+  int32_t part_tokens;  // tokens per split-K partition
+  int32_t max_parts;    // partial slots per (sequence, kv head) in the workspace
+  int32_t out_bf16;     // 1: bf16 output, 0: fp32
+  float scale_log2;     // softmax scale * log2(e)
+  // dynamic shared memory carve-up (byte offsets)
+  int32_t off_sc;
+  int32_t off_red;
+  int32_t off_tbl;
+  int32_t off_prefix;
+  int32_t off_bar;
+  // workspace carve-up
+  int32_t* ws_err;
+  int32_t* ws_counters;
+  float* ws_ml;
+  float* ws_o;
+};
+
+// Per (dtype, head_dim, group) kernel entry: shared memory need and launch.
+struct DecodeKernelInfo {
+  const void* fn;
+  int ring_bytes;   // kStages * stage allocation
+  int tokens_per_stage;
+  int q_bytes;
+};
+
+// Returns false if the combination is not compiled.
+bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInfo* info);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
+                                     const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                     int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                     int32_t row_bytes, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks,
+                               int64_t block_bytes, const int64_t* pairs, int32_t num_pairs,
+                               cudaStream_t stream);
+
+}  // namespace pa

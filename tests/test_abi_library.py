@@ -1,0 +1,69 @@
+"""The C-ABI library loads on a host without a GPU and exports every symbol
+include/pa.h declares; host-only calls behave as documented."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for n in ("pa_reshape_and_cache", "pa_decode", "pa_copy_blocks", "pa_decode_workspace_size",
+              "pa_alloc_create", "pa_alloc_append_slot", "pa_alloc_fork"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from paged_kv_cache_142_gb300 import _lib
+    names = declared_functions()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(_lib.SIGNATURES) == names  # the binding declares exactly the header's calls
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert lib.pa_status_string(4) == b"PA_ERR_OOM"
+    assert b"sm_103a" in lib.pa_version()
+
+
+def test_workspace_size_plan_is_host_only(lib):
+    # split-K workspace for a long context is larger than for a short one
+    small = lib.pa_decode_workspace_size(8, 64, 8, 128, 16, 1, 256, 0)
+    big = lib.pa_decode_workspace_size(8, 64, 8, 128, 16, 1, 32768, 0)
+    assert 0 < small < big
+    # 8 seqs * 8 kv heads * 128 partitions * 8 heads * (128 + 2) floats, plus header/counters
+    assert big >= 8 * 8 * 128 * 8 * 130 * 4
+    # unsupported group size -> 0
+    assert lib.pa_decode_workspace_size(1, 48, 2, 128, 16, 1, 100, 0) == 0
+    pt = C.c_int32(0)
+    st = lib.pa_decode_plan(8, 64, 8, 128, 16, 1, 32768, 0, C.byref(pt), None)
+    assert st == 0 and pt.value == 256
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    from paged_kv_cache_142_gb300 import _lib as L
+    # bad block size / head_dim / dtype are rejected on the host
+    assert lib.pa_reshape_and_cache(None, None, 1, None, None, None, 8, 12, 2, 128, 1, None) == L.PA_ERR_UNSUPPORTED
+    assert lib.pa_copy_blocks(None, None, 8, 16, 2, 128, 7, None, 1, None) == L.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(None, None, 0, None, None, None, 8, 16, 2, 128, 1, None) == L.PA_OK
+    # missing pointers with work to do
+    assert lib.pa_reshape_and_cache(None, None, 3, None, None, None, 8, 16, 2, 128, 1, None) == L.PA_ERR_INVALID_ARG
+    # num_q_heads not a multiple of num_kv_heads
+    rc = lib.pa_decode(None, 0, None, 2, 6, None, None, 8, 16, 4, 128, 1, None, 4, None, 64,
+                       1.0, 0, None, 0, None)
+    assert rc == L.PA_ERR_INVALID_ARG
+    # table too short for max_context_len
+    rc = lib.pa_decode(None, 0, None, 2, 8, None, None, 8, 16, 4, 128, 1, None, 2, None, 64,
+                       1.0, 0, None, 0, None)
+    assert rc == L.PA_ERR_INVALID_ARG
