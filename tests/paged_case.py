@@ -27,6 +27,12 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+def raw_bits(a: np.ndarray) -> np.ndarray:
+    """Element bit patterns of a host array of bf16 bits or float32 values."""
+    a = np.ascontiguousarray(a)
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
 def cache_bits(t: torch.Tensor) -> np.ndarray:
     t = t.detach().cpu()
     if t.dtype == torch.bfloat16:
@@ -95,8 +101,8 @@ class OracleState:
             t = self.alloc.block_table(i)
             self.tables[i, :len(t)] = t
         shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
-        src_k = wl.key_hist.bits if bits else wl.key_hist.f32
-        src_v = wl.value_hist.bits if bits else wl.value_hist.f32
+        src_k = raw_bits(wl.key_hist.bits) if bits else wl.key_hist.f32
+        src_v = raw_bits(wl.value_hist.bits) if bits else wl.value_hist.f32
         dt = src_k.dtype if bits else np.float64
         self.k_cache = np.zeros(shape, dtype=dt)
         self.v_cache = np.zeros(shape, dtype=dt)

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from paged_kv_cache_142_gb300 import workloads as W
-from paged_case import GpuState, OracleState, cache_bits, to_device
+from paged_case import GpuState, OracleState, cache_bits, raw_bits, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -37,10 +37,11 @@ def test_slot_write_skips_padding_and_out_of_range(ops, dtype):
     kc = torch.zeros((NB, Hkv, bs, D), dtype=dt, device="cuda")
     vc = torch.zeros_like(kc)
     ops.pa_reshape_and_cache(to_device(key), to_device(val), torch.from_numpy(slots).cuda(), kc, vc)
-    ek = np.zeros((NB, Hkv, bs, D), dtype=key.bits.dtype)
+    kb, vb = raw_bits(key.bits), raw_bits(val.bits)
+    ek = np.zeros((NB, Hkv, bs, D), dtype=kb.dtype)
     ev = np.zeros_like(ek)
     keep = (slots >= 0) & (slots < NB * bs)
-    oracle.reshape_and_cache(key.bits[keep], val.bits[keep], ek, ev, slots[keep])
+    oracle.reshape_and_cache(kb[keep], vb[keep], ek, ev, slots[keep])
     assert np.array_equal(cache_bits(kc), ek)
     assert np.array_equal(cache_bits(vc), ev)
 
@@ -57,7 +58,7 @@ def test_copy_blocks_bit_exact(ops, dtype, bs, Hkv, D):
     kc = to_device(k).contiguous()
     vc = to_device(v).contiguous()
     ops.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).cuda())
-    ek, ev = k.bits.copy(), v.bits.copy()
+    ek, ev = raw_bits(k.bits).copy(), raw_bits(v.bits).copy()
     oracle.copy_blocks(ek, ev, pairs)
     assert np.array_equal(cache_bits(kc), ek)
     assert np.array_equal(cache_bits(vc), ev)
