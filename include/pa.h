@@ -17,7 +17,8 @@
  *     block_size*head_dim contiguous elements; one whole block across kv heads
  *     is contiguous too.  Both base pointers must be 16-byte aligned.
  *   - Every pointer named "device" is a CUDA device pointer owned by the
- *     caller; the library never allocates, frees or keeps device memory.
+ *     caller; the library never allocates, frees or keeps device memory,
+ *     except the fixed scratch array of pa_decode_no_alloc.
  *     "host" pointers are read or written before the call returns.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
  *     work is enqueued asynchronously on it; the call does not synchronise.
@@ -150,6 +151,34 @@ pa_status pa_decode(void* out, pa_dtype out_dtype,
                     float scale, int32_t partition_tokens,
                     void* workspace, size_t workspace_bytes,
                     void* stream);
+
+/* pa_decode without a caller workspace, for callers that cannot allocate
+ * device memory: code running inside another runtime whose memory pool owns
+ * the device memory, plugin hooks that may only use the buffers they are
+ * handed, and latency-critical loops that cannot afford the device
+ * synchronisation cudaMalloc/cudaFree may imply.  The pages have no
+ * counterpart for this call; it exists only for such callers.
+ *
+ * Arguments and result as pa_decode, minus the workspace.  The scratch is a
+ * fixed 32 MiB array in the library's device memory, held by every GPU that
+ * loads the library until the process exits.  With partition_tokens == 0 the
+ * partitions are enlarged until the scratch suffices; PA_ERR_WORKSPACE if it
+ * cannot (a fixed partition_tokens whose workspace exceeds 32 MiB, or more
+ * than about 8 million (sequence, kv head) pairs).  The call allocates
+ * nothing.  Its first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call shares the one array and zeroes its
+ * bookkeeping words first, so calls that overlap on the GPU (other streams,
+ * other host threads) race and corrupt each other: issue them in one stream
+ * order.  Device-side status (pa_workspace_error) is not reported. */
+pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype,
+                             const void* q, int32_t num_seqs, int32_t num_q_heads,
+                             const void* k_cache, const void* v_cache,
+                             int32_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len,
+                             float scale, int32_t partition_tokens, void* stream);
 
 /* Partition size and CTA count pa_decode would use (host only; either out
  * pointer may be NULL). */

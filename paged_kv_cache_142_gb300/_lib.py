@@ -38,6 +38,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (C.c_size_t, [i32, i32, i32, i32, i32, i32, i32, i32]),
     "pa_decode": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32,
                         C.c_float, i32, vp, C.c_size_t, vp]),
+    "pa_decode_no_alloc": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32,
+                                 vp, i32, C.c_float, i32, vp]),
     "pa_decode_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, P_i32, P_i32]),
     "pa_workspace_init": (i32, [vp, C.c_size_t, vp]),
     "pa_workspace_error": (i32, [vp, vp, P_i32]),

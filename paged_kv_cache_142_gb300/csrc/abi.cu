@@ -320,3 +320,71 @@ pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_stat
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Paged decode for callers that cannot allocate device memory.
+//
+// Some callers of this library cannot call cudaMalloc: code that runs inside
+// another runtime whose memory pool already owns the device memory (a stray
+// allocation would fail or fragment that pool), plugin hooks that may only
+// use the buffers they are handed, and latency-critical loops where the
+// implicit device synchronisation of cudaMalloc/cudaFree is not acceptable.
+// For them pa_decode_no_alloc runs the same decode kernel with its scratch in
+// the file-scope device array below instead of a caller workspace.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+extern "C" pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
+                                        int32_t num_seqs, int32_t num_q_heads,
+                                        const void* k_cache, const void* v_cache,
+                                        int32_t num_blocks, int32_t block_size,
+                                        int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t max_context_len,
+                                        float scale, int32_t partition_tokens, void* stream) {
+  // Device address of the scratch array on the current device, looked up once
+  // per device (the host-side symbol is only a stand-in, not a device address).
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // Plan; with automatic partitions, enlarge them until the scratch fits.
+  Plan pl;
+  int32_t pt = partition_tokens;
+  pa_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                           max_context_len, pt, &pl);
+  if (st != PA_OK) return st;
+  while (pl.ws_total > kNoAllocScratchBytes) {
+    if (partition_tokens > 0 || pl.max_parts == 1) return PA_ERR_WORKSPACE;
+    pt = pl.part_tokens * 2;
+    st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                   max_context_len, pt, &pl);
+    if (st != PA_OK) return st;
+  }
+  if (num_seqs == 0) return PA_OK;
+  // The array keeps the previous call's contents: zero the error word and the
+  // per-(sequence, kv head) counters, which must start at zero.
+  if (cudaMemsetAsync(scratch, 0, pl.ws_ml, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return pa_decode(out, out_dtype, q, num_seqs, num_q_heads, k_cache, v_cache, num_blocks,
+                   block_size, num_kv_heads, head_dim, dtype, block_tables, max_blocks_per_seq,
+                   context_lens, max_context_len, scale, pt, scratch, kNoAllocScratchBytes, stream);
+}

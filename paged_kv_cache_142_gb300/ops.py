@@ -129,6 +129,28 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_k
             "pa_decode")
 
 
+def pa_decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       max_context_len, partition_tokens=0, stream=None) -> None:
+    """pa_decode with the library's fixed device scratch instead of a workspace,
+    for callers that cannot allocate device memory (see include/pa.h)."""
+    NB, Hkv, bs, D = _cache_dims(k_cache, v_cache)
+    _need(Hkv == num_kv_heads, "num_kv_heads does not match the cache")
+    B, H, Dq = q.shape
+    _need(Dq == D and q.dtype == k_cache.dtype and q.is_contiguous(), "q must be [B, H, D] in the cache dtype")
+    _need(out.shape == q.shape and out.is_contiguous() and out.dtype in (torch.float32, torch.bfloat16),
+          "out must be a contiguous [B, H, D] fp32 or bf16 tensor")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B
+          and block_tables.is_contiguous(), "block_tables must be contiguous int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == B, "context_lens must be int32 [B]")
+    L.check(_LIB.pa_decode_no_alloc(out.data_ptr(), dtype_code(out.dtype), q.data_ptr(), B, H,
+                                    k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
+                                    dtype_code(k_cache.dtype), block_tables.data_ptr(),
+                                    block_tables.shape[1], context_lens.data_ptr(),
+                                    int(max_context_len), float(scale), int(partition_tokens),
+                                    _stream(stream)),
+            "pa_decode_no_alloc")
+
+
 def pa_workspace_init(workspace, stream=None) -> None:
     L.check(_LIB.pa_workspace_init(workspace.data_ptr(), workspace.numel(), _stream(stream)),
             "pa_workspace_init")
