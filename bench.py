@@ -260,7 +260,7 @@ def gpu_arm(args):
     B_.build(quiet=True)
     from paged_kv_cache_142_gb300 import ops
 
-    wl = W.gqa_bf16()
+    wl = W.gqa_bf16(num_seqs=args.num_seqs)
     B, H, Hkv, D, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     e = W.elem_bytes(wl.dtype)
     K, Wm = args.steps, args.warmup
@@ -335,16 +335,43 @@ def gpu_arm(args):
     dev_status = ops.pa_workspace_error(ws)
     if dev_status != 0:
         raise RuntimeError(f"device status {dev_status} after the timed steps")
+    if args.profile:
+        # profiling case: device-resident steps only
+        sampler.stop()
+        print(json.dumps({"profile": True, "num_seqs": B, "steps": K, "ms_per_step": total_ms / K,
+                          "decode_ms": statistics.mean(dec_ms),
+                          "decode_gbs": decode_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9,
+                          "decode_bytes": decode_bytes}), flush=True)
+        return
 
     # ---------------- end to end through the C ABI, host buffers ----------------
+    # The e2e leg replays the last R decode steps of every sequence: a fresh
+    # allocator state holds max(1, len - R) history tokens per sequence, and
+    # each timed step reserves one more slot per sequence on the host,
+    # copies that step's inputs from pinned host memory, runs the kernels and
+    # reads the output back.  Pinned input buffers alternate between two sets
+    # so the host never overwrites one an earlier copy still reads.
+    R = min(K, 128)
+    e2e_warm = min(Wm, 3)
+    alloc2 = ops.BlockAllocator(NB, bs, free_order)
+    seqs2 = [alloc2.seq_create() for _ in range(B)]
+    start_len = np.maximum(1, wl.context_lens.astype(np.int64) - R)
+    hist2 = np.concatenate([alloc2.append_tokens(s, int(n)) for s, n in zip(seqs2, start_len)])
+    sel = np.concatenate([np.arange(st[i], st[i] + start_len[i]) for i in range(B)])
+    ops.pa_reshape_and_cache(
+        torch.from_numpy(np.ascontiguousarray(wl.key_hist.bits[sel])).view(torch.bfloat16).to(dev),
+        torch.from_numpy(np.ascontiguousarray(wl.value_hist.bits[sel])).view(torch.bfloat16).to(dev),
+        torch.from_numpy(hist2).to(dev), kc, vc)
+    torch.cuda.synchronize(dev)
     pin = dict(pin_memory=True)
     h_q = torch.from_numpy(np.ascontiguousarray(wl.q.bits)).view(torch.bfloat16).pin_memory()
     h_k = new_k.cpu().pin_memory()
     h_v = new_v.cpu().pin_memory()
-    h_slots = torch.empty(B, dtype=torch.int64, **pin)
-    h_tables = torch.empty((B, maxb), dtype=torch.int32, **pin)
-    h_lens = torch.empty(B, dtype=torch.int32, **pin)
-    h_out = torch.empty((B, H, D), dtype=torch.bfloat16, **pin)
+    hb = [dict(slots=torch.empty(B, dtype=torch.int64, **pin),
+               tables=torch.empty((B, maxb), dtype=torch.int32, **pin),
+               lens=torch.empty(B, dtype=torch.int32, **pin),
+               out=torch.empty((B, H, D), dtype=torch.bfloat16, **pin)) for _ in range(2)]
+    copied = [None, None]
     d_q = torch.empty_like(q)
     d_k = torch.empty_like(new_k)
     d_v = torch.empty_like(new_v)
@@ -352,43 +379,49 @@ def gpu_arm(args):
     d_tables = torch.empty_like(t_tables)
     d_lens = torch.empty_like(t_lens)
     d_pairs = torch.empty((B, 2), dtype=torch.int64, device=dev)
-    # the device-timed steps rewrote the last token in place; the e2e leg
-    # appends new tokens after it
+    h_pairs = torch.empty((B, 2), dtype=torch.int64, **pin)
+    d_out = torch.empty_like(out)
     e2e_bytes = []
-    n_cow = 0
+    counter = [0]
 
     def e2e_step():
-        nonlocal n_cow
-        slots, pairs = alloc.append_slots(seqs)        # host allocator: reserve slots
-        tb, ln = alloc.export_tables(seqs, maxb)
-        h_slots.numpy()[:] = slots
-        h_tables.numpy()[:] = tb
-        h_lens.numpy()[:] = ln
+        j = counter[0] % 2
+        counter[0] += 1
+        b = hb[j]
+        if copied[j] is not None:
+            copied[j].synchronize()                    # the copies that read this set are done
+        slots, pairs = alloc2.append_slots(seqs2)      # host allocator: reserve the slots
+        tb, ln = alloc2.export_tables(seqs2, maxb)
+        b["slots"].numpy()[:] = slots
+        b["tables"].numpy()[:] = tb
+        b["lens"].numpy()[:] = ln
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        d_tables.copy_(h_tables, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
-        if len(pairs):
-            d_pairs[:len(pairs)].copy_(torch.from_numpy(pairs))
+        d_slots.copy_(b["slots"], non_blocking=True)
+        d_tables.copy_(b["tables"], non_blocking=True)
+        d_lens.copy_(b["lens"], non_blocking=True)
+        if len(pairs):                                 # copy-on-write (none in this workload)
+            h_pairs.numpy()[:len(pairs)] = pairs
+            d_pairs[:len(pairs)].copy_(h_pairs[:len(pairs)], non_blocking=True)
             ops.pa_copy_blocks(kc, vc, d_pairs[:len(pairs)])
-            n_cow += len(pairs)
+        ev_c = torch.cuda.Event()
+        ev_c.record(stream)
+        copied[j] = ev_c
         ops.pa_reshape_and_cache(d_k, d_v, d_slots, kc, vc)
         ops.pa_decode(d_out, d_q, kc, vc, d_tables, d_lens, wl.scale, Hkv, e2e_max_len, ws)
-        h_out.copy_(d_out, non_blocking=True)
+        b["out"].copy_(d_out, non_blocking=True)       # the step's result back to the host
         return ln
 
-    d_out = torch.empty_like(out)
-    for _ in range(min(Wm, 3)):
-        ln = e2e_step()
+    for _ in range(e2e_warm):
+        e2e_step()
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w2 = time.time()
     e0.record(stream)
-    for _ in range(K):
+    for _ in range(R):
         ln = e2e_step()
         e2e_bytes.append(sum(step_bytes(ln, B, H, Hkv, D, e, 2)))
     e1.record(stream)
@@ -400,14 +433,13 @@ def gpu_arm(args):
     if ops.pa_workspace_error(ws) != 0:
         raise RuntimeError("device status after the e2e steps")
 
-    h2d = (h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_slots.numel() * 8
-           + h_tables.numel() * 4 + h_lens.numel() * 4)
-    d2h = h_out.numel() * 2
+    h2d = (h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + B * 8 + B * maxb * 4 + B * 4)
+    d2h = B * H * D * 2
 
     # max over ranks
     t_step = total_ms / K
     t_dec = statistics.mean(dec_ms)
-    t_e2e = e2e_ms / K
+    t_e2e = e2e_ms / R
     vals = [t_step, t_dec, t_e2e]
     if world > 1:
         tt = torch.tensor(vals, dtype=torch.float64, device=dev)
@@ -459,7 +491,8 @@ def gpu_arm(args):
         "pct_of_nominal_8tbs": round(100 * achieved / 8000.0, 2),
         "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "seq_steps_per_s": round(world * B / (t_e2e * 1e-3), 1),
-                "ms_per_step": round(t_e2e, 5)},
+                "ms_per_step": round(t_e2e, 5), "steps": R,
+                "note": "last R decode steps of each sequence, host allocator in the loop"},
         "gpu_launches": 2 * K,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -480,6 +513,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=256,
+                    help="batch size (the benchmark workload is 256; smaller for profiling)")
+    ap.add_argument("--profile", action="store_true",
+                    help="device-resident steps only (no e2e leg, no CPU baseline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
