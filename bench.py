@@ -260,7 +260,7 @@ def gpu_arm(args):
     B_.build(quiet=True)
     from paged_kv_cache_142_gb300 import ops
 
-    wl = W.gqa_bf16(num_seqs=args.num_seqs)
+    wl = W.gqa_bf16(num_seqs=args.num_seqs, block_size=args.block_size)
     B, H, Hkv, D, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     e = W.elem_bytes(wl.dtype)
     K, Wm = args.steps, args.warmup
@@ -296,7 +296,7 @@ def gpu_arm(args):
     t_lens = torch.from_numpy(lens).to(dev)
     t_slots = torch.from_numpy(new_slots).to(dev)
     out = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
-    ws = ops.make_workspace(B, H, Hkv, D, bs, "bf16", e2e_max_len, device=dev)
+    ws = ops.make_workspace(B, H, Hkv, D, bs, "bf16", e2e_max_len, args.partition_tokens, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -307,7 +307,8 @@ def gpu_arm(args):
 
     def step():
         ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
-        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws)
+        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws,
+                      partition_tokens=args.partition_tokens)
 
     # ---------------- device-resident steps ----------------
     for _ in range(Wm):
@@ -322,7 +323,8 @@ def gpu_arm(args):
     for k in range(K):
         ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
         ev[k][0].record(stream)
-        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws)
+        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws,
+                      partition_tokens=args.partition_tokens)
         ev[k][1].record(stream)
     t1e.record(stream)
     torch.cuda.synchronize(dev)
@@ -339,6 +341,8 @@ def gpu_arm(args):
         # profiling case: device-resident steps only
         sampler.stop()
         print(json.dumps({"profile": True, "num_seqs": B, "steps": K, "ms_per_step": total_ms / K,
+                          "partition_tokens": ops.pa_decode_plan(B, H, Hkv, D, bs, "bf16", e2e_max_len,
+                                                                 args.partition_tokens)[0],
                           "decode_ms": statistics.mean(dec_ms),
                           "decode_gbs": decode_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9,
                           "decode_bytes": decode_bytes}), flush=True)
@@ -409,7 +413,8 @@ def gpu_arm(args):
         ev_c.record(stream)
         copied[j] = ev_c
         ops.pa_reshape_and_cache(d_k, d_v, d_slots, kc, vc)
-        ops.pa_decode(d_out, d_q, kc, vc, d_tables, d_lens, wl.scale, Hkv, e2e_max_len, ws)
+        ops.pa_decode(d_out, d_q, kc, vc, d_tables, d_lens, wl.scale, Hkv, e2e_max_len, ws,
+                      partition_tokens=args.partition_tokens)
         b["out"].copy_(d_out, non_blocking=True)       # the step's result back to the host
         return ln
 
@@ -456,7 +461,7 @@ def gpu_arm(args):
     value = world * step_b / (t_step * 1e-3) / 1e9
     achieved = decode_bytes / (t_dec * 1e-3) / 1e9
     e2e_val = world * statistics.mean(e2e_bytes) / (t_e2e * 1e-3) / 1e9
-    pt, ctas = ops.pa_decode_plan(B, H, Hkv, D, bs, "bf16", e2e_max_len)
+    pt, ctas = ops.pa_decode_plan(B, H, Hkv, D, bs, "bf16", e2e_max_len, args.partition_tokens)
     clocks = sampler.summary()
 
     cpu = None
@@ -515,6 +520,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=256,
                     help="batch size (the benchmark workload is 256; smaller for profiling)")
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="KV block size in tokens (the benchmark workload uses 16)")
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="split-K partition size passed to pa_decode (0 = automatic)")
     ap.add_argument("--profile", action="store_true",
                     help="device-resident steps only (no e2e leg, no CPU baseline)")
     args = ap.parse_args()

@@ -1,5 +1,8 @@
 // C ABI shim: argument validation, split-K planning, workspace carve-up and
 // launches on the caller's stream.  Declarations and contracts: include/pa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -44,8 +47,16 @@ pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_
   return PA_OK;
 }
 
+// Tensor-core kernel layout constants (must match decode_umma.cuh).
+constexpr int kUmmaThreadsHost = 192;
+constexpr int kUmmaTileBytesHost = 32768;
+constexpr int kUmmaBarriersHost = 2 * 8 + 13;
+
 struct Plan {
   DecodeKernelInfo info;
+  bool umma;       // tensor-core kernel (bf16, head_dim 128, block >= 8)
+  int stages;
+  int off_q, off_p, off_small;
   int group;
   int part_tokens;
   int max_parts;
@@ -64,32 +75,64 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   if (dtype_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
   if (!is_pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
   const int G = num_q_heads / num_kv_heads;
-  if (!pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
-    return PA_ERR_UNSUPPORTED;
+  std::memset(pl, 0, sizeof(*pl));
   pl->group = G;
-  // partition size: a multiple of the block size and of the stage; at most
-  // part/2 partitions per sequence (the merge stages 2 floats per partition
-  // and head in the score buffer)
-  const int64_t gran = block_size > pl->info.tokens_per_stage ? block_size : pl->info.tokens_per_stage;
+  // bf16 K/V with head_dim 128 and blocks of >= 8 tokens run on the tensor
+  // cores; everything else on the CUDA-core kernel
+  pl->umma = dtype == PA_DTYPE_BF16 && head_dim == 128 && block_size >= 32 &&
+             pa::decode_umma_fn(G) != nullptr;
+  if (!pl->umma && !pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
+    return PA_ERR_UNSUPPORTED;
+  // partition size: a multiple of the block size and of the stage (tensor
+  // cores: of the 128-token tile); at most part/2 partitions per sequence
+  const int64_t unit = pl->umma ? 128 : pl->info.tokens_per_stage;
+  const int64_t gran = block_size > unit ? block_size : unit;
   int64_t pt = round_up(partition_tokens > 0 ? partition_tokens : kDefaultPartTokens, gran);
   while (ceil_div(max_context_len, pt) > pt / 2) pt *= 2;
   if (pt > (1 << 20)) return PA_ERR_UNSUPPORTED;
   pl->part_tokens = static_cast<int>(pt);
   pl->max_parts = static_cast<int>(ceil_div(max_context_len, pt) > 1 ? ceil_div(max_context_len, pt) : 1);
   // shared memory
-  int64_t off = pl->info.ring_bytes;
-  pl->off_sc = static_cast<int>(off);
-  off += round_up(pt * G * 4, 16);
-  pl->off_red = static_cast<int>(off);
-  off += round_up((static_cast<int64_t>(pa::kConsumerWarps) * G * head_dim + 2 * pa::kConsumerWarps * G + 2 * G) * 4, 16);
-  pl->off_tbl = static_cast<int>(off);
-  off += round_up((pt / block_size + 1) * 4, 16);
-  pl->off_prefix = static_cast<int>(off);
-  off += round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
-  pl->off_bar = static_cast<int>(off);
-  off += 2 * pa::kStages * 8;
-  if (off + 64 > kMaxSmem) return PA_ERR_UNSUPPORTED;  // + static shared memory
-  pl->smem = static_cast<int>(off);
+  if (pl->umma) {
+    const int64_t tail = round_up(kUmmaBarriersHost * 8 + 16, 16) +
+                         round_up((pt / block_size + 1) * 4, 16) +
+                         round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
+    int stages = 6;
+    auto total_for = [&](int ns) {
+      return static_cast<int64_t>(ns) * kUmmaTileBytesHost + 2 * 4096 + 2 * 8192 + 1024 + tail + 1024;
+    };
+    while (stages > 3 && total_for(stages) + 64 > kMaxSmem) --stages;
+    if (total_for(stages) + 64 > kMaxSmem) return PA_ERR_UNSUPPORTED;
+    pl->stages = stages;
+    int64_t off = static_cast<int64_t>(stages) * kUmmaTileBytesHost;
+    pl->off_q = static_cast<int>(off);
+    off += 2 * 4096;
+    pl->off_p = static_cast<int>(off);
+    off += 2 * 8192;
+    pl->off_small = static_cast<int>(off);
+    off += 1024;
+    pl->off_bar = static_cast<int>(off);
+    off += round_up(kUmmaBarriersHost * 8 + 16, 16);
+    pl->off_tbl = static_cast<int>(off);
+    off += round_up((pt / block_size + 1) * 4, 16);
+    pl->off_prefix = static_cast<int>(off);
+    off += round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
+    pl->smem = static_cast<int>(off + 1024);  // slack to align the base to 1024 bytes
+  } else {
+    int64_t off = pl->info.ring_bytes;
+    pl->off_sc = static_cast<int>(off);
+    off += round_up(pt * G * 4, 16);
+    pl->off_red = static_cast<int>(off);
+    off += round_up((static_cast<int64_t>(pa::kConsumerWarps) * G * head_dim + 2 * pa::kConsumerWarps * G + 2 * G) * 4, 16);
+    pl->off_tbl = static_cast<int>(off);
+    off += round_up((pt / block_size + 1) * 4, 16);
+    pl->off_prefix = static_cast<int>(off);
+    off += round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
+    pl->off_bar = static_cast<int>(off);
+    off += 2 * pa::kStages * 8;
+    if (off + 64 > kMaxSmem) return PA_ERR_UNSUPPORTED;  // + static shared memory
+    pl->smem = static_cast<int>(off);
+  }
   // workspace: header | counters | (max, sum) partials | output partials
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_kv_heads;
   pl->ws_counters = 256;
@@ -106,6 +149,39 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   return PA_OK;
 }
 
+const void* plan_kernel(const Plan& pl) { return pl.umma ? pa::decode_umma_fn(pl.group) : pl.info.fn; }
+int plan_threads(const Plan& pl) { return pl.umma ? kUmmaThreadsHost : pa::kDecodeThreads; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D map over rows of 128 bf16 (256 bytes): boxes of 64 elements (one
+// 128-byte swizzle span) by box_rows rows.
+bool encode_rows_128(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Per-kernel dynamic shared memory attribute and occupancy, cached.
 struct KernelCache {
   const void* fn;
@@ -118,7 +194,7 @@ std::mutex g_mu;
 KernelCache g_cache[64];
 int g_ncache = 0;
 
-pa_status prepare_kernel(const void* fn, int smem, int* ctas) {
+pa_status prepare_kernel(const void* fn, int threads, int smem, int* ctas) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -137,7 +213,7 @@ pa_status prepare_kernel(const void* fn, int smem, int* ctas) {
   }
   if (kc->smem_occ != smem) {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, pa::kDecodeThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, smem) !=
         cudaSuccess)
       return PA_ERR_CUDA;
     kc->occ = occ;
@@ -225,7 +301,7 @@ pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   if (partition_tokens_out) *partition_tokens_out = pl.part_tokens;
   if (num_ctas_out) {
     int ctas = 0;
-    st = prepare_kernel(pl.info.fn, pl.smem, &ctas);
+    st = prepare_kernel(plan_kernel(pl), plan_threads(pl), pl.smem, &ctas);
     if (st != PA_OK) return st;
     *num_ctas_out = ctas;
   }
@@ -256,7 +332,7 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
   if (!workspace || workspace_bytes < pl.ws_total || !aligned16(workspace))
     return PA_ERR_WORKSPACE;
   int ctas = 0;
-  st = prepare_kernel(pl.info.fn, pl.smem, &ctas);
+  st = prepare_kernel(plan_kernel(pl), plan_threads(pl), pl.smem, &ctas);
   if (st != PA_OK) return st;
   const int64_t max_items = static_cast<int64_t>(num_seqs) * num_kv_heads * pl.max_parts;
   if (ctas > max_items) ctas = static_cast<int>(max_items);
@@ -280,6 +356,10 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
   p.max_parts = pl.max_parts;
   p.out_bf16 = out_dtype == PA_DTYPE_BF16 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.stages = pl.stages;
+  p.off_q = pl.off_q;
+  p.off_p = pl.off_p;
+  p.off_small = pl.off_small;
   p.off_sc = pl.off_sc;
   p.off_red = pl.off_red;
   p.off_tbl = pl.off_tbl;
@@ -291,10 +371,27 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
   p.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   p.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
 
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(pl.info.fn, dim3(static_cast<unsigned>(ctas)),
-                                   dim3(pa::kDecodeThreads), args, static_cast<size_t>(pl.smem),
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (pl.umma) {
+    // TMA tensor maps over the K and V pools (rows of 128 dims, one box per
+    // block and 64-dim half) and over the queries (one box per GQA group)
+    const int64_t cache_rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
+    const int64_t q_rows = static_cast<int64_t>(num_seqs) * num_q_heads;
+    if (cache_rows >= (int64_t(1) << 31) || q_rows >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv, tmq;
+    const uint32_t box_rows = static_cast<uint32_t>(block_size < 128 ? block_size : 128);
+    if (!encode_rows_128(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
+        !encode_rows_128(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
+        !encode_rows_128(&tmq, q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(pl.group)))
+      return PA_ERR_CUDA;
+    void* args[] = {&p, &tmk, &tmv, &tmq};
+    e = cudaLaunchKernel(plan_kernel(pl), dim3(static_cast<unsigned>(ctas)), dim3(kUmmaThreadsHost),
+                         args, static_cast<size_t>(pl.smem), static_cast<cudaStream_t>(stream));
+  } else {
+    void* args[] = {&p};
+    e = cudaLaunchKernel(pl.info.fn, dim3(static_cast<unsigned>(ctas)), dim3(pa::kDecodeThreads),
+                         args, static_cast<size_t>(pl.smem), static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

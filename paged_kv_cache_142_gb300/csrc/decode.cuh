@@ -37,6 +37,10 @@ struct DecodeParams {
   int32_t out_bf16;     // 1: bf16 output, 0: fp32
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared memory carve-up (byte offsets)
+  int32_t stages;  // ring depth of the tensor-core kernel
+  int32_t off_q;
+  int32_t off_p;
+  int32_t off_small;
   int32_t off_sc;
   int32_t off_red;
   int32_t off_tbl;
@@ -59,6 +63,9 @@ struct DecodeKernelInfo {
 
 // Returns false if the combination is not compiled.
 bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInfo* info);
+
+// Tensor-core kernel (bf16, head_dim 128) for a GQA group, or nullptr.
+const void* decode_umma_fn(int group);
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
