@@ -47,7 +47,7 @@ WORKLOAD = ("paged decode step (KV append + decode), batch 256, 32 q / 8 kv head
             "pool 1.2x needed, values N(0,1)*0.5")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_gqa_bf16_b256.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_142_gb300", "csrc", f)
-                  for f in ("decode_kernel.cuh", "decode.cuh", "ptx.cuh")]
+                  for f in ("decode_umma.cuh", "decode_common.cuh", "decode.cuh", "ptx.cuh")]
 
 
 def kernel_hash() -> str:

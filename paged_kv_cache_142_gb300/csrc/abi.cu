@@ -28,6 +28,7 @@ using pa::DecodeParams;
 
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kDefaultPartTokens = 256;
+constexpr int64_t kSmCountHint = 152;  // GB300 SMs; only shapes the default partition size
 
 int dtype_bytes(pa_dtype d) {
   return d == PA_DTYPE_F32 ? 4 : (d == PA_DTYPE_BF16 ? 2 : 0);
@@ -48,15 +49,15 @@ pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_
 }
 
 // Tensor-core kernel layout constants (must match decode_umma.cuh).
-constexpr int kUmmaThreadsHost = 192;
+constexpr int kUmmaThreadsHost = 384;
 constexpr int kUmmaTileBytesHost = 32768;
-constexpr int kUmmaBarriersHost = 2 * 8 + 13;
 
 struct Plan {
   DecodeKernelInfo info;
   bool umma;       // tensor-core kernel (bf16, head_dim 128, block >= 8)
-  int stages;
-  int off_q, off_p, off_small;
+  int stages, stages_v;
+  int tbl_stride;
+  int off_q, off_p, off_small, off_lens;
   int group;
   int part_tokens;
   int max_parts;
@@ -79,7 +80,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   pl->group = G;
   // bf16 K/V with head_dim 128 and blocks of >= 8 tokens run on the tensor
   // cores; everything else on the CUDA-core kernel
-  pl->umma = dtype == PA_DTYPE_BF16 && head_dim == 128 && block_size >= 32 &&
+  pl->umma = dtype == PA_DTYPE_BF16 && head_dim == 128 && block_size >= 8 &&
              pa::decode_umma_fn(G) != nullptr;
   if (!pl->umma && !pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
     return PA_ERR_UNSUPPORTED;
@@ -87,38 +88,62 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   // cores: of the 128-token tile); at most part/2 partitions per sequence
   const int64_t unit = pl->umma ? 128 : pl->info.tokens_per_stage;
   const int64_t gran = block_size > unit ? block_size : unit;
-  int64_t pt = round_up(partition_tokens > 0 ? partition_tokens : kDefaultPartTokens, gran);
+  // tensor cores: long partitions (few epilogues and merges), halved while the
+  // (sequence, kv head, partition) items would not give every SM two; CUDA
+  // cores: 256
+  int64_t def_pt = kDefaultPartTokens;
+  if (pl->umma) {
+    def_pt = 2048;
+    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    while (def_pt > 256 && units * ceil_div(max_context_len, def_pt) < 2 * kSmCountHint) def_pt /= 2;
+  }
+  int64_t pt = round_up(partition_tokens > 0 ? partition_tokens : def_pt, gran);
   while (ceil_div(max_context_len, pt) > pt / 2) pt *= 2;
   if (pt > (1 << 20)) return PA_ERR_UNSUPPORTED;
   pl->part_tokens = static_cast<int>(pt);
   pl->max_parts = static_cast<int>(ceil_div(max_context_len, pt) > 1 ? ceil_div(max_context_len, pt) : 1);
   // shared memory
   if (pl->umma) {
-    const int64_t tail = round_up(kUmmaBarriersHost * 8 + 16, 16) +
-                         round_up((pt / block_size + 1) * 4, 16) +
-                         round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
-    int stages = 6;
-    auto total_for = [&](int ns) {
-      return static_cast<int64_t>(ns) * kUmmaTileBytesHost + 2 * 4096 + 2 * 8192 + 1024 + tail + 1024;
-    };
-    while (stages > 3 && total_for(stages) + 64 > kMaxSmem) --stages;
-    if (total_for(stages) + 64 > kMaxSmem) return PA_ERR_UNSUPPORTED;
-    pl->stages = stages;
-    int64_t off = static_cast<int64_t>(stages) * kUmmaTileBytesHost;
-    pl->off_q = static_cast<int>(off);
-    off += 2 * 4096;
-    pl->off_p = static_cast<int>(off);
-    off += 2 * 8192;
-    pl->off_small = static_cast<int>(off);
-    off += 1024;
-    pl->off_bar = static_cast<int>(off);
-    off += round_up(kUmmaBarriersHost * 8 + 16, 16);
-    pl->off_tbl = static_cast<int>(off);
-    off += round_up((pt / block_size + 1) * 4, 16);
-    pl->off_prefix = static_cast<int>(off);
-    off += round_up((static_cast<int64_t>(num_seqs) + 1) * 4, 16);
-    pl->smem = static_cast<int>(off + 1024);  // slack to align the base to 1024 bytes
-  } else {
+    // K ring | V ring | queries [2 groups] | P [2 groups][2] | per-group
+    // scratch | barriers, flags | table slices [2 streams][2 groups] |
+    // lengths | prefix | align slack
+    const int64_t pbytes = G <= 8 ? 4096 : 8192;
+    const int64_t tbl_stride = round_up(pt / block_size + 1, 4);
+    const int64_t fixed = 2 * 4096 + 2 * 2 * pbytes + 2 * 1024 + 256 + 1024 + 4 * tbl_stride * 4 +
+                          round_up(static_cast<int64_t>(num_seqs) * 4, 16) +
+                          2 * round_up((static_cast<int64_t>(num_seqs) + 4) / 4 * 4 * 4, 16) + 1024;
+    int sk = 3, sv = 3;
+    while (sk + sv > 4 && (sk + sv) * kUmmaTileBytesHost + fixed > kMaxSmem) {
+      if (sv > sk) --sv; else --sk;
+    }
+    if ((sk + sv) * kUmmaTileBytesHost + fixed > kMaxSmem) {
+      pl->umma = false;  // too many sequences for one CTA's shared memory: CUDA cores
+    } else {
+      pl->stages = sk;
+      pl->stages_v = sv;
+      pl->tbl_stride = static_cast<int>(tbl_stride);
+      int64_t off = static_cast<int64_t>(sk + sv) * kUmmaTileBytesHost;
+      pl->off_q = static_cast<int>(off);
+      off += 2 * 4096;
+      pl->off_p = static_cast<int>(off);
+      off += 2 * 2 * pbytes;
+      pl->off_small = static_cast<int>(off);
+      off += 2 * 1024 + 256;  // per-group scratch, then the two item queues
+      pl->off_bar = static_cast<int>(off);
+      off += 1024;
+      pl->off_tbl = static_cast<int>(off);  // [K/V stream][group]
+      off += 4 * tbl_stride * 4;
+      pl->off_lens = static_cast<int>(off);
+      off += round_up(static_cast<int64_t>(num_seqs) * 4, 16);
+      pl->off_prefix = static_cast<int>(off);  // two prefix arrays of (num_seqs + 4) & ~3 ints
+      off += 2 * round_up((static_cast<int64_t>(num_seqs) + 4) / 4 * 4 * 4, 16);
+      pl->smem = static_cast<int>(off + 1024);  // slack to align the base to 1024 bytes
+    }
+  }
+  if (!pl->umma && !pl->info.fn &&
+      !pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
+    return PA_ERR_UNSUPPORTED;
+  if (!pl->umma) {
     int64_t off = pl->info.ring_bytes;
     pl->off_sc = static_cast<int>(off);
     off += round_up(pt * G * 4, 16);
@@ -357,6 +382,9 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
   p.out_bf16 = out_dtype == PA_DTYPE_BF16 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.stages = pl.stages;
+  p.stages_v = pl.stages_v;
+  p.tbl_stride = pl.tbl_stride;
+  p.off_lens = pl.off_lens;
   p.off_q = pl.off_q;
   p.off_p = pl.off_p;
   p.off_small = pl.off_small;

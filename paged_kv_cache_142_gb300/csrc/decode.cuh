@@ -37,7 +37,10 @@ struct DecodeParams {
   int32_t out_bf16;     // 1: bf16 output, 0: fp32
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared memory carve-up (byte offsets)
-  int32_t stages;  // ring depth of the tensor-core kernel
+  int32_t stages;      // K ring depth of the tensor-core kernel
+  int32_t stages_v;    // V ring depth of the tensor-core kernel
+  int32_t tbl_stride;  // table-slice entries per compute group (tensor-core kernel)
+  int32_t off_lens;
   int32_t off_q;
   int32_t off_p;
   int32_t off_small;

@@ -64,11 +64,13 @@ __device__ __forceinline__ void store_out(void* out, int bf16, int64_t i, float 
 // Work items are (sequence, kv head, partition); sequence i owns
 // max(1, ceil(len_i / part_tokens)) * num_kv_heads of them, enumerated
 // sequence-major, partition-major, kv head fastest.  Every thread of the CTA
-// calls this; prefix[0..num_seqs] receives the exclusive prefix sum and the
-// CTA is synchronised on return.  CTA 0 reports lengths outside
+// calls this; prefix[0..num_seqs] receives the exclusive prefix sum (and
+// lens_out, if given, the clamped lengths) and the CTA is synchronised on
+// return.  CTA 0 reports lengths outside
 // [0, max_context_len] in the workspace error word.
 __device__ __forceinline__ void build_item_prefix(const DecodeParams& p, int32_t* prefix,
-                                                  int* warp_sums, int tid, int nthreads) {
+                                                  int* warp_sums, int tid, int nthreads,
+                                                  int32_t* lens_out = nullptr) {
   const int nseq = p.num_seqs;
   const int pt = p.part_tokens;
   const int hkv = p.num_kv_heads;
@@ -81,6 +83,7 @@ __device__ __forceinline__ void build_item_prefix(const DecodeParams& p, int32_t
     const int raw = p.context_lens[i];
     if (blockIdx.x == 0 && (raw < 0 || raw > p.max_context_len)) atomicExch(p.ws_err, kDevErrInvalidArg);
     const int len = clamp_len(raw, p.max_context_len);
+    if (lens_out) lens_out[i] = len;
     local += max(1, (len + pt - 1) / pt) * hkv;
   }
   int x = local;

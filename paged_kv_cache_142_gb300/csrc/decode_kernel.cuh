@@ -406,13 +406,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         p.ws_ml[rec * G * 2 + 2 * ctid] = m;
         p.ws_ml[rec * G * 2 + 2 * ctid + 1] = l;
       }
+      // release: every writer orders its partial stores before the barrier;
+      // the counting thread acquires right after the atomic and only then
+      // publishes the result
       __threadfence();
       ptx::bar_sync(1, kConsumerThreads);
-      if (ctid == 0) flags[1] = (atomicAdd(&p.ws_counters[row], 1) == nparts - 1) ? 1 : 0;
+      if (ctid == 0) {
+        const int arrived = atomicAdd(&p.ws_counters[row], 1);
+        __threadfence();
+        flags[1] = (arrived == nparts - 1) ? 1 : 0;
+      }
       ptx::bar_sync(1, kConsumerThreads);
       if (flags[1]) {
         // last partition of this (sequence, kv head) to finish: merge
-        __threadfence();
         const float* mlrow = p.ws_ml + static_cast<int64_t>(row) * p.max_parts * G * 2;
         const float* orow = p.ws_o + static_cast<int64_t>(row) * p.max_parts * G * D;
         float* wm = sc;                // [nparts * G]: max, then merge weights

@@ -6,35 +6,49 @@
 // names for logical block t / block_size; softmax(scale q.K) V over the
 // history).  The GQA group turns both products into dense tiles:
 //   S^T[128 tokens x 16] = K_tile[128 x 128 dims] . Q^T[128 dims x 16 heads]
-//   O^T[128 dims x 16]  += V_tile^T[128 dims x 128 tokens] . P^T[128 tokens x 16]
-// (heads padded to N = 16), each a handful of tcgen05.mma instructions with
-// fp32 accumulators in tensor memory.  P enters the second product as two
-// bf16 terms, hi = bf16(p) and lo = bf16(p - hi), side by side in the B tile
-// (columns 0..7 and 8..15 for G <= 8, N = 32 for G = 16), so the result
-// keeps about 16 bits of each probability instead of bf16's 8.
+//   O^T[128 dims x N]   += V_tile^T[128 dims x 128 tokens] . P^T[128 tokens x N]
+// (heads padded to 16), each a handful of tcgen05.mma instructions with fp32
+// accumulators in tensor memory.  P enters the second product as two bf16
+// terms, hi = bf16(p) and lo = bf16(p - hi), side by side in the B tile
+// (N = 16: columns 0..7 and 8..15 for G <= 8; N = 32 for G = 16), so the
+// result keeps about 16 bits of each probability instead of bf16's 8.
 //
-// Warp roles (one CTA per SM, persistent over (sequence, kv head, partition)
-// work items enumerated from context_lens in shared memory):
-//  * warp 0 streams: per item it hoists the partition's block-table slice
-//    into shared memory, loads the query rows with a TMA tensor copy, and for
-//    every 128-token tile issues TMA tensor copies (128-byte swizzle, L2
-//    evict-first) of each block's K rows, then V rows, into a ring of 32 KB
-//    stages;
-//  * warp 1 owns 64 tensor-memory columns (S and O, double-buffered) and one
-//    lane issues the MMAs: Q.K of tile u+1 goes out before P.V of tile u so
-//    the score tile of the next tile is ready while softmax runs;
-//  * warps 2-5 (one thread per token row, then per head-dim row): online
-//    softmax in fp32 on the score tile (block max via shuffles + shared
-//    memory, exp2 in the log2 domain), P written to shared memory as bf16,
-//    rescale-and-accumulate of each tile's P.V in registers, and the item's
-//    epilogue: store, or write (max, sum, unnormalised O) and, in the last
-//    CTA to finish a (sequence, kv head), merge the partitions by
-//    log-sum-exp.
+// One CTA per SM, persistent over (sequence, kv head, partition) work items.
+// Items are enumerated from context_lens in shared memory, full partitions
+// first and the shorter last partitions after them, and claimed
+// dynamically: the K-stream warp takes the next item index from a global
+// counter in the workspace whenever one of the CTA's two compute groups
+// needs work, and publishes it to that group's queue in shared memory,
+// which every other role reads in order.  The two groups' 128-token tiles
+// are interleaved into one stream (group 0 tile, group 1 tile, ...) that
+// every stream-walking warp derives identically.  The K path and the V path run decoupled,
+// each with its own ring of 32 KB stages, streaming warp and MMA warp:
+//  * warp 0 streams K: per item it hoists the partition's block-table slice
+//    into shared memory (cp.async, issued as soon as the item is known, into
+//    a double-buffered slice) and loads the query rows (TMA tensor copy);
+//    per tile
+//    it issues, from one lane per block, TMA tensor copies (128-byte swizzle,
+//    L2 evict-first) of that block's K rows into the K ring;
+//  * warp 10 streams V the same way into the V ring;
+//  * warp 1 owns the tensor memory (per group: S and O, double-buffered) and
+//    one lane issues Q.K^T of every tile as soon as its K tile has landed;
+//  * warp 11 issues P.V of every tile once its V tile has landed and its P
+//    is ready (zeroing first the V rows past the end of a sequence inside
+//    the tile's last 16-token step);
+//  * warps 2-5 and 6-9 are the two compute groups (one thread per token row,
+//    then per head-dim row): online softmax in fp32 on the score tile (block
+//    max via shuffles + shared memory, exp2 in the log2 domain), P written to
+//    shared memory as bf16 hi/lo, rescale-and-accumulate of each tile's P.V
+//    in registers, and the item's epilogue: store, or write (max, sum,
+//    unnormalised O) and, in the last CTA to finish a (sequence, kv head),
+//    merge the partitions by log-sum-exp.
 // Rows past the end of a sequence: their scores are masked, their P is 0,
 // V rows inside the last 16-token MMA step are zeroed in shared memory, and
 // later steps are not issued, so stale or uninitialised memory never enters
-// the sums.  All mbarrier waits are bounded; on expiry every role stops,
-// the MMA lane drains its work, tensor memory is freed and
+// the sums.  Every mbarrier wait is made by a role that consumed the
+// previous phase of the same barrier itself, so no parity wait can alias a
+// phase two ahead.  All mbarrier waits are bounded; on expiry every role stops,
+// the MMA lanes drain their work, tensor memory is freed and
 // PA_ERR_DEVICE_TIMEOUT is written to the workspace.
 #pragma once
 
@@ -44,47 +58,231 @@
 
 namespace pa {
 
-constexpr int kUmmaThreads = 192;
-constexpr int kUmmaTile = 128;          // tokens per tile (MMA M)
-constexpr int kUmmaTileBytes = 32768;   // one K or V tile: 2 halves x 128 rows x 128 B
+constexpr int kUmmaThreads = 384;        // 0 K stream, 1 Q.K MMA, 2-9 compute, 10 V stream, 11 P.V MMA
+constexpr int kUmmaTile = 128;           // tokens per tile (MMA M)
+constexpr int kUmmaTileBytes = 32768;    // one K or V tile: 2 halves x 128 rows x 128 B
 constexpr int kUmmaMaxStages = 8;
-constexpr int kUmmaQBytes = 4096;       // query tile: 2 halves x 16 rows x 128 B
-constexpr int kUmmaPBytes = 8192;       // P tile: 128 tokens x (hi, lo) x up to 16 heads x bf16
-constexpr int kUmmaSmallBytes = 1024;   // reductions and rescale factors
-constexpr int kUmmaBarriers = 2 * kUmmaMaxStages + 13;
-// tensor memory: S[2] at columns 0 and 16; O[2] (hi and lo halves) from column 32
+constexpr int kUmmaQBytes = 4096;        // query tile: 2 halves x 16 rows x 128 B (one per group)
+constexpr int kUmmaSmallBytes = 1024;    // per group: reductions and rescale factors
+constexpr int kUmmaGroupBars = 16;
+constexpr int kUmmaQueue = 8;            // per-group item queue depth
+constexpr int kUmmaQueueReaders = 7;     // V stream, Q.K warp, P.V warp, 4 compute warps
+constexpr int kUmmaBarriers = 4 * kUmmaMaxStages + 2 * kUmmaGroupBars + 2 + 4 * kUmmaQueue;
+
+__host__ __device__ constexpr int umma_p_bytes(int G) { return G <= 8 ? 4096 : 8192; }
 
 namespace umma_detail {
 
-enum Bar : int {
-  kFull = 0,
-  kEmpty = kUmmaMaxStages,
-  kQFull = 2 * kUmmaMaxStages,
-  kQEmpty = kQFull + 2,
-  kSFull = kQEmpty + 2,
-  kSEmpty = kSFull + 2,
-  kPFull = kSEmpty + 2,
-  kPEmpty = kPFull + 2,
-  kOFull = kPEmpty + 2,
-  kOEmpty = kOFull + 2,
-  kDrain = kOEmpty + 2,
-};
+// barrier indices: K ring, V ring, per-group blocks, drains
+constexpr int kKFull = 0;
+constexpr int kKEmpty = kUmmaMaxStages;
+constexpr int kVFull = 2 * kUmmaMaxStages;
+constexpr int kVEmpty = 3 * kUmmaMaxStages;
+constexpr int kGroup0 = 4 * kUmmaMaxStages;
+// within a group's block of kUmmaGroupBars
+constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kSEmpty = 6, kPFull = 8, kPEmpty = 10,
+              kOFull = 12, kOEmpty = 14;
+constexpr int kDrainQK = 4 * kUmmaMaxStages + 2 * kUmmaGroupBars;
+constexpr int kDrainPV = kDrainQK + 1;
+constexpr int kItemFull = kDrainPV + 1;                   // [group][kUmmaQueue]
+constexpr int kItemEmpty = kItemFull + 2 * kUmmaQueue;    // [group][kUmmaQueue]
 
 struct Item {
   int seq, kvh, part, len, t0, ntok, nparts;
 };
 
-__device__ __forceinline__ Item item_at(const DecodeParams& p, const int32_t* prefix, int w) {
+// Item enumeration: first every full partition (part_tokens tokens) of
+// every sequence, sequence-major, kv head fastest; then every sequence's
+// last, shorter partition (or its single empty item when len == 0).
+// prefix_full / prefix_tail hold the exclusive prefix sums of the per
+// sequence item counts of the two phases.
+struct Ctx {
+  const DecodeParams* p;
+  const int32_t* prefix_full;
+  const int32_t* prefix_tail;
+  const int32_t* lens;
+  int n_full, total;
+};
+
+// First s with prefix[s + 1] > w (prefix non-decreasing, prefix[0] = 0).
+__device__ __forceinline__ int seq_of(int w, const int32_t* prefix, int nseq) {
+  int lo = 0, hi = nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid + 1] > w) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Item item_at(const Ctx& c, int w) {
   Item it;
-  decode_detail::find_item(w, prefix, p.num_seqs, p.num_kv_heads, it.seq, it.kvh, it.part);
-  it.len = decode_detail::clamp_len(p.context_lens[it.seq], p.max_context_len);
-  it.t0 = it.part * p.part_tokens;
-  it.ntok = min(it.len - it.t0, p.part_tokens);
-  it.nparts = it.len > 0 ? (it.len + p.part_tokens - 1) / p.part_tokens : 1;
+  const int hkv = c.p->num_kv_heads;
+  const int pt = c.p->part_tokens;
+  if (w < c.n_full) {
+    it.seq = seq_of(w, c.prefix_full, c.p->num_seqs);
+    const int u = w - c.prefix_full[it.seq];
+    it.part = u / hkv;
+    it.kvh = u - it.part * hkv;
+  } else {
+    const int v = w - c.n_full;
+    it.seq = seq_of(v, c.prefix_tail, c.p->num_seqs);
+    it.kvh = v - c.prefix_tail[it.seq];
+    it.part = c.lens[it.seq] / pt;
+  }
+  it.len = c.lens[it.seq];
+  it.t0 = it.part * pt;
+  it.ntok = min(it.len - it.t0, pt);
+  it.nparts = it.len > 0 ? (it.len + pt - 1) / pt : 1;
   return it;
 }
 
-// bounded wait; once a CTA has given up, later waits are skipped
+// Builds lens, prefix_full and prefix_tail; every thread calls it; the CTA
+// is synchronised on return.  CTA 0 reports lengths outside
+// [0, max_context_len] in the workspace error word.
+__device__ __forceinline__ void build_two_phase_prefix(const DecodeParams& p, int32_t* lens,
+                                                       int32_t* prefix_full, int32_t* prefix_tail,
+                                                       int* warp_sums, int tid, int nthreads) {
+  const int nseq = p.num_seqs, pt = p.part_tokens, hkv = p.num_kv_heads;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  const int per = (nseq + nthreads - 1) / nthreads;
+  const int beg = min(nseq, tid * per);
+  const int end = min(nseq, beg + per);
+  int lf = 0, lt = 0;
+  for (int i = beg; i < end; ++i) {
+    const int raw = p.context_lens[i];
+    if (blockIdx.x == 0 && (raw < 0 || raw > p.max_context_len)) atomicExch(p.ws_err, kDevErrInvalidArg);
+    const int len = decode_detail::clamp_len(raw, p.max_context_len);
+    lens[i] = len;
+    lf += (len / pt) * hkv;
+    lt += (len % pt != 0 || len == 0) ? hkv : 0;
+  }
+  int xf = lf, xt = lt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int yf = __shfl_up_sync(0xffffffffu, xf, off);
+    const int yt = __shfl_up_sync(0xffffffffu, xt, off);
+    if (lane >= off) {
+      xf += yf;
+      xt += yt;
+    }
+  }
+  if (lane == 31) {
+    warp_sums[warp] = xf;
+    warp_sums[nwarps + warp] = xt;
+  }
+  __syncthreads();
+  int rf = xf - lf, rt = xt - lt;
+  for (int w = 0; w < warp; ++w) {
+    rf += warp_sums[w];
+    rt += warp_sums[nwarps + w];
+  }
+  for (int i = beg; i < end; ++i) {
+    const int len = lens[i];
+    prefix_full[i] = rf;
+    prefix_tail[i] = rt;
+    rf += (len / pt) * hkv;
+    rt += (len % pt != 0 || len == 0) ? hkv : 0;
+  }
+  if (tid == nthreads - 1) {
+    prefix_full[nseq] = rf;
+    prefix_tail[nseq] = rt;
+  }
+  __syncthreads();
+}
+
+// One compute group's item sequence, as published in its queue.
+struct GroupIter {
+  int j, nt;
+  uint32_t k;      // queue entries consumed so far
+  uint32_t items;  // non-empty items started so far (query slot phase)
+  bool valid;
+  Item it;
+};
+
+// One tile of the merged stream.
+struct Rec {
+  int g;          // compute group
+  Item it;
+  int j, nt, nv;  // tile index in the item, tiles of the item, valid rows
+  uint32_t u;     // tile index in the CTA's stream (stage u % depth of each ring)
+  uint32_t ug;    // tile index within the group (S/P/O buffers)
+  uint32_t qi;    // item index within the group (query slot phase)
+};
+
+// Next item of group g from `next_w(g, k)` (the publisher claims and
+// publishes, readers read the queue); empty items go to on_empty.
+template <typename NextW, typename OnEmpty>
+__device__ __forceinline__ void seek(const Ctx& c, GroupIter& s, int g, NextW&& next_w,
+                                     OnEmpty&& on_empty) {
+  while (true) {
+    const int w = next_w(g, s.k++);
+    if (w < 0) break;
+    s.it = item_at(c, w);
+    if (s.it.ntok > 0) {
+      s.nt = (s.it.ntok + kUmmaTile - 1) / kUmmaTile;
+      s.j = 0;
+      s.valid = true;
+      return;
+    }
+    on_empty(g, s.it);
+  }
+  s.valid = false;
+}
+
+struct Stream {
+  GroupIter a, b;  // the two groups' item iterators (named: no dynamic indexing)
+  int turn;
+  uint32_t u, ua, ub;
+
+  template <typename NextW, typename OnEmpty>
+  __device__ __forceinline__ void init(const Ctx& c, NextW&& next_w, OnEmpty&& on_empty) {
+    a.k = a.items = 0;
+    b.k = b.items = 0;
+    seek(c, a, 0, next_w, on_empty);
+    seek(c, b, 1, next_w, on_empty);
+    turn = 0;
+    u = ua = ub = 0;
+  }
+
+  template <typename NextW, typename OnEmpty>
+  __device__ __forceinline__ void take(const Ctx& c, GroupIter& s, int g, uint32_t& ug, Rec& r,
+                                       NextW&& next_w, OnEmpty&& on_empty) {
+    r.g = g;
+    r.it = s.it;
+    r.j = s.j;
+    r.nt = s.nt;
+    r.nv = min(kUmmaTile, s.it.ntok - s.j * kUmmaTile);
+    r.u = u++;
+    r.ug = ug++;
+    r.qi = s.items;
+    if (++s.j == s.nt) {
+      ++s.items;
+      seek(c, s, g, next_w, on_empty);
+    }
+    turn = g ^ 1;
+  }
+
+  template <typename NextW, typename OnEmpty>
+  __device__ __forceinline__ bool next(const Ctx& c, Rec& r, NextW&& next_w, OnEmpty&& on_empty) {
+    // alternate groups; when one group has no work left, take from the other
+    const bool use_b = turn ? b.valid : !a.valid;
+    if (use_b) {
+      if (!b.valid) return false;
+      take(c, b, 1, ub, r, next_w, on_empty);
+    } else {
+      if (!a.valid) return false;
+      take(c, a, 0, ua, r, next_w, on_empty);
+    }
+    return true;
+  }
+};
+
+struct NoOp {
+  __device__ __forceinline__ void operator()(int, const Item&) const {}
+};
+
+// bounded wait; once a role has given up, later waits are skipped
 __device__ __forceinline__ void wait(uint64_t* bar, uint32_t parity, bool& aborted) {
   if (!aborted && !ptx::mbar_wait(bar, parity, kWaitLimitNs)) aborted = true;
 }
@@ -105,205 +303,295 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   using namespace umma_detail;
   static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
   constexpr int HD = 128;
-  constexpr int NP = G <= 8 ? 16 : 32;        // P.V columns: hi heads, then lo heads
-  constexpr int LO = NP / 2;                  // column of the lo half
-  constexpr int PGRP = NP / 8;                // 8-column core matrices per P row group
-  constexpr uint32_t TMEM_COLS = G <= 8 ? 64 : 128;
+  constexpr int NP = G <= 8 ? 16 : 32;     // P.V columns: hi heads, then lo heads
+  constexpr int LO = NP / 2;               // column of the lo half
+  constexpr int PGRP = NP / 8;             // 8-column core matrices per P row group
+  constexpr int PB = umma_p_bytes(G);      // one P buffer
+  constexpr uint32_t TMEM_COLS = G <= 8 ? 128 : 256;  // S[2][2] x 16, then O[2][2] x NP
 
   extern __shared__ unsigned char smem_raw[];
-  __shared__ int warp_sums[kUmmaThreads / 32];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  unsigned char* ring = smem;
-  unsigned char* qbuf = smem + p.off_q;
-  unsigned char* pbuf = smem + p.off_p;
-  float* red_m = reinterpret_cast<float*>(smem + p.off_small);  // [2][4][16]
-  float* red_l = red_m + 2 * 4 * 16;                            // [4][16]
-  float* alpha_s = red_l + 4 * 16;                              // [2][16]
+  const int NSK = p.stages;                 // K ring stages
+  const int NSV = p.stages_v;               // V ring stages
+  unsigned char* kring = smem;
+  unsigned char* vring = smem + NSK * kUmmaTileBytes;
+  unsigned char* qbuf = smem + p.off_q;    // [group] x 4 KB
+  unsigned char* pbuf = smem + p.off_p;    // [group][buffer] x PB
+  unsigned char* small = smem + p.off_small;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kUmmaBarriers);
-  // [0] stream/MMA gave up, [1] merge this item, [2] compute warps gave up
+  // [0] a streaming or MMA role gave up, [1..2] group merges its item,
+  // [3..4] group gave up
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* tbl = reinterpret_cast<int32_t*>(smem + p.off_tbl);
-  int32_t* prefix = reinterpret_cast<int32_t*>(smem + p.off_prefix);
+  int* warp_sums = const_cast<int*>(flags) + 5;   // 2 x 12 ints
+  int32_t* tbl = reinterpret_cast<int32_t*>(smem + p.off_tbl);  // [K/V stream][group][tbl_stride]
+  int32_t* lens = reinterpret_cast<int32_t*>(smem + p.off_lens);
+  int32_t* prefix_full = reinterpret_cast<int32_t*>(smem + p.off_prefix);
+  int32_t* prefix_tail = prefix_full + ((p.num_seqs + 4) & ~3);
+  volatile int* queue = reinterpret_cast<volatile int*>(small + 2 * kUmmaSmallBytes);  // [group][kUmmaQueue]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int NS = p.stages;
   const int hkv = p.num_kv_heads;
   const int bs = p.block_size;
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(&bars[kFull + s], 1);
-      ptx::mbar_init(&bars[kEmpty + s], 1);
+    for (int s = 0; s < NSK; ++s) {
+      ptx::mbar_init(&bars[kKFull + s], 1);
+      ptx::mbar_init(&bars[kKEmpty + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&bars[kQFull + b], 1);
-      ptx::mbar_init(&bars[kQEmpty + b], 1);
-      ptx::mbar_init(&bars[kSFull + b], 1);
-      ptx::mbar_init(&bars[kSEmpty + b], 4);
-      ptx::mbar_init(&bars[kPFull + b], 4);
-      ptx::mbar_init(&bars[kPEmpty + b], 1);
-      ptx::mbar_init(&bars[kOFull + b], 1);
-      ptx::mbar_init(&bars[kOEmpty + b], 4);
+    for (int s = 0; s < NSV; ++s) {
+      ptx::mbar_init(&bars[kVFull + s], 1);
+      ptx::mbar_init(&bars[kVEmpty + s], 1);
     }
-    ptx::mbar_init(&bars[kDrain], 1);
-    flags[0] = 0;
-    flags[1] = 0;
-    flags[2] = 0;
+    for (int g = 0; g < 2; ++g) {
+      uint64_t* gb = bars + kGroup0 + g * kUmmaGroupBars;
+      ptx::mbar_init(&gb[kQFull], 1);   // one query slot per group
+      ptx::mbar_init(&gb[kQEmpty], 1);
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(&gb[kSFull + b], 1);
+        ptx::mbar_init(&gb[kSEmpty + b], 4);
+        ptx::mbar_init(&gb[kPFull + b], 4);
+        ptx::mbar_init(&gb[kPEmpty + b], 1);
+        ptx::mbar_init(&gb[kOFull + b], 1);
+        ptx::mbar_init(&gb[kOEmpty + b], 4);
+      }
+    }
+    ptx::mbar_init(&bars[kDrainQK], 1);
+    ptx::mbar_init(&bars[kDrainPV], 1);
+    for (int q = 0; q < 2 * kUmmaQueue; ++q) {
+      ptx::mbar_init(&bars[kItemFull + q], 1);
+      ptx::mbar_init(&bars[kItemEmpty + q], kUmmaQueueReaders);
+    }
+    for (int i = 0; i < 5; ++i) flags[i] = 0;
     ptx::mbar_init_fence();
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, TMEM_COLS);
     ptx::tc_fence_before();
   }
-  decode_detail::build_item_prefix(p, prefix, warp_sums, tid, kUmmaThreads);  // syncs the CTA
+  build_two_phase_prefix(p, lens, prefix_full, prefix_tail, warp_sums, tid, kUmmaThreads);  // syncs
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = prefix[p.num_seqs];
+  const int n_full = prefix_full[p.num_seqs];
+  const Ctx ctx{&p, prefix_full, prefix_tail, lens, n_full, n_full + prefix_tail[p.num_seqs]};
   bool aborted = false;
+  int* item_counter = p.ws_err + 1;   // next unclaimed item (all CTAs)
+  int* done_counter = p.ws_err + 2;   // CTAs finished
 
-  if (warp == 0) {
-    // ============================ TMA streaming ============================
+  // Readers of group g's queue: lane 0 waits for entry k, reads it and
+  // frees it; the warp gets it by shuffle.  -1 ends the group.
+  auto read_item = [&](int g, uint32_t k) -> int {
+    int w = -1;
     if (lane == 0) {
-      ptx::prefetch_tensormap(&tm_k);
-      ptx::prefetch_tensormap(&tm_v);
-      ptx::prefetch_tensormap(&tm_q);
+      const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
+      wait(&bars[kItemFull + slot], (k / kUmmaQueue) & 1u, aborted);
+      if (!aborted) w = queue[slot];
+      ptx::mbar_arrive(&bars[kItemEmpty + slot]);
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
+  };
+
+  if (warp == 0 || warp == 10) {
+    // ============================ TMA streaming ============================
+    // warp 0: query rows and K tiles; warp 10: V tiles
+    const bool is_v = warp == 10;
+    if (lane == 0) {
+      ptx::prefetch_tensormap(is_v ? &tm_v : &tm_k);
+      if (!is_v) ptx::prefetch_tensormap(&tm_q);
     }
     const uint64_t pol_kv = ptx::policy_evict_first();
     const uint64_t pol_q = ptx::policy_evict_normal();
+    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+    unsigned char* ring = is_v ? vring : kring;
+    uint64_t* full = bars + (is_v ? kVFull : kKFull);
+    uint64_t* empty = bars + (is_v ? kVEmpty : kKEmpty);
+    const int NS = is_v ? NSV : NSK;
     const int box_rows = min(bs, kUmmaTile);
-    uint32_t u = 0, qi = 0;
-    for (int w = blockIdx.x; w < total && !aborted; w += gridDim.x) {
-      const Item it = item_at(p, prefix, w);
-      if (it.ntok <= 0) continue;
-      const int b0 = it.t0 / bs;
-      const int nb = (it.t0 + it.ntok + bs - 1) / bs - b0;
-      const int32_t* trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq + b0;
-      for (int j = lane; j < nb; j += 32) {
-        int phys = trow[j];
+    // warp 0 claims items for both groups and publishes them; warp 10 reads.
+    // A claim is made only when a group needs its next item, so no CTA
+    // holds work another could start sooner.
+    auto publish_item = [&](int g, uint32_t k) -> int {
+      int w = -1;
+      if (lane == 0) {
+        const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
+        wait(&bars[kItemEmpty + slot], ((k / kUmmaQueue) & 1u) ^ 1u, aborted);
+        if (!aborted) {
+          w = atomicAdd(item_counter, 1);
+          if (w >= ctx.total) w = -1;
+        }
+        queue[slot] = w;
+        ptx::mbar_arrive(&bars[kItemFull + slot]);
+      }
+      return __shfl_sync(0xffffffffu, w, 0);
+    };
+    auto next_w = [&](int g, uint32_t k) -> int { return is_v ? read_item(g, k) : publish_item(g, k); };
+    // block-table slice of the group's current item, [stream][group] in shared memory
+    auto slice = [&](int g) -> int32_t* { return tbl + ((is_v ? 2 : 0) + g) * p.tbl_stride; };
+    Stream st;
+    st.init(ctx, next_w, NoOp{});
+    Rec r;
+    while (!aborted && st.next(ctx, r, next_w, NoOp{})) {
+      int32_t* gtbl = slice(r.g);
+      const int b0 = r.it.t0 / bs;
+      if (r.j == 0) {
+        const int nb = (r.it.t0 + r.it.ntok + bs - 1) / bs - b0;
+        const int32_t* trow = p.block_tables + static_cast<int64_t>(r.it.seq) * p.max_blocks_per_seq + b0;
+        for (int j = lane; j < nb; j += 32) gtbl[j] = trow[j];
+        __syncwarp();
+        if (!is_v && lane == 0) {
+          uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
+          wait(&gb[kQEmpty], (r.qi & 1u) ^ 1u, aborted);
+          ptx::mbar_arrive_expect_tx(&gb[kQFull], 2u * G * 128u);
+          unsigned char* qd = qbuf + r.g * kUmmaQBytes;
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_2d(qd + h * 2048, &tm_q, 64 * h, r.it.seq * p.num_q_heads + r.it.kvh * G,
+                             &gb[kQFull], pol_q);
+        }
+      }
+      // this lane's block of the tile (lanes < nbox)
+      const int tok0 = r.it.t0 + r.j * kUmmaTile;
+      const int nbox = (r.nv + box_rows - 1) / box_rows;
+      int row = 0;
+      if (lane < nbox) {
+        const int tok = tok0 + lane * box_rows;
+        const int lb = tok / bs;
+        int phys = gtbl[lb - b0];
         if (phys < 0 || phys >= p.num_blocks) {  // never read outside the pool
           atomicExch(p.ws_err, kDevErrInvalidArg);
           phys = 0;
         }
-        tbl[j] = phys;
+        row = (phys * hkv + r.it.kvh) * bs + (tok - lb * bs);
+      }
+      const int slot = static_cast<int>(r.u % NS);
+      if (lane == 0) {
+        wait(&empty[slot], ((r.u / NS) & 1u) ^ 1u, aborted);
+        ptx::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * box_rows * 256));
+      }
+      aborted = __shfl_sync(0xffffffffu, aborted, 0);
+      if (!aborted && lane < nbox) {
+        unsigned char* dst = ring + slot * kUmmaTileBytes + lane * box_rows * 128;
+        ptx::tma_load_2d(dst, tm, 0, row, &full[slot], pol_kv);
+        ptx::tma_load_2d(dst + 16384, tm, 64, row, &full[slot], pol_kv);
       }
       __syncwarp();
-      const int nt = (it.ntok + kUmmaTile - 1) / kUmmaTile;
-      if (lane == 0) {
-        const uint32_t qs = qi & 1u;
-        wait(&bars[kQEmpty + qs], ((qi >> 1) & 1u) ^ 1u, aborted);
-        ptx::mbar_arrive_expect_tx(&bars[kQFull + qs], 2u * G * 128u);
-        for (int h = 0; h < 2; ++h)
-          ptx::tma_load_2d(qbuf + qs * kUmmaQBytes + h * 2048, &tm_q, 64 * h,
-                           it.seq * p.num_q_heads + it.kvh * G, &bars[kQFull + qs], pol_q);
-        for (int j = 0; j < nt && !aborted; ++j) {
-          const int tok0 = it.t0 + j * kUmmaTile;
-          const int nv = min(kUmmaTile, it.ntok - j * kUmmaTile);
-          const int nbox = (nv + box_rows - 1) / box_rows;
-          for (int kv = 0; kv < 2; ++kv) {
-            const uint32_t e = 2u * (u + j) + kv;
-            const int slot = static_cast<int>(e % NS);
-            wait(&bars[kEmpty + slot], ((e / NS) & 1u) ^ 1u, aborted);
-            ptx::mbar_arrive_expect_tx(&bars[kFull + slot], static_cast<uint32_t>(nbox * box_rows * 256));
-            unsigned char* dst = ring + slot * kUmmaTileBytes;
-            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-            for (int bi = 0; bi < nbox; ++bi) {
-              const int tok = tok0 + bi * box_rows;
-              const int lb = tok / bs;
-              const int row = (tbl[lb - b0] * hkv + it.kvh) * bs + (tok - lb * bs);
-              for (int h = 0; h < 2; ++h)
-                ptx::tma_load_2d(dst + h * 16384 + bi * box_rows * 128, tm, 64 * h, row,
-                                 &bars[kFull + slot], pol_kv);
-            }
-          }
-        }
-      }
-      u += nt;
-      ++qi;
-      aborted = __shfl_sync(0xffffffffu, aborted, 0);
-      __syncwarp();  // the table slice is rewritten by the next item
     }
   } else if (warp == 1) {
-    // ============================ MMA issue ============================
+    // ============================ Q.K^T issue ============================
     if (lane == 0) {
       constexpr uint32_t kIdQK = ptx::idesc_bf16_f32(128, 16, 0, 0);
-      constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, NP, 1, 1);
-      bool have_prev = false;
-      uint32_t prev_u = 0;
-      int prev_nv = 0;
-      auto issue_pv = [&](uint32_t pu, int pnv) {
-        const uint32_t e = 2u * pu + 1u;
-        const int vslot = static_cast<int>(e % NS);
-        const uint32_t b = pu & 1u;
-        wait(&bars[kFull + vslot], (e / NS) & 1u, aborted);
-        wait(&bars[kPFull + b], (pu >> 1) & 1u, aborted);
-        wait(&bars[kOEmpty + b], ((pu >> 1) & 1u) ^ 1u, aborted);
+      auto read_one = [&](int g, uint32_t k) -> int {
+        const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
+        wait(&bars[kItemFull + slot], (k / kUmmaQueue) & 1u, aborted);
+        const int w = aborted ? -1 : queue[slot];
+        ptx::mbar_arrive(&bars[kItemEmpty + slot]);
+        return w;
+      };
+      Stream st;
+      st.init(ctx, read_one, NoOp{});
+      Rec r;
+      while (!aborted && st.next(ctx, r, read_one, NoOp{})) {
+        uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
+        const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
+        if (r.j == 0) wait(&gb[kQFull], r.qi & 1u, aborted);
+        const int kslot = static_cast<int>(r.u % NSK);
+        wait(&bars[kKFull + kslot], (r.u / NSK) & 1u, aborted);
+        wait(&gb[kSEmpty + b], ph ^ 1u, aborted);
         ptx::tc_fence_after();
-        const unsigned char* vt = ring + vslot * kUmmaTileBytes;
-        const unsigned char* pt = pbuf + b * kUmmaPBytes;
-        const int nks = (pnv + 15) / 16;
+        const unsigned char* kt = kring + kslot * kUmmaTileBytes;
+        const unsigned char* qt = qbuf + r.g * kUmmaQBytes;
+        const uint32_t sd = tmem + (r.g * 2 + b) * 16;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int h = kk >> 2, k4 = kk & 3;
+          ptx::umma_bf16(sd, ptx::smem_desc(kt + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
+                         ptx::smem_desc(qt + h * 2048 + k4 * 32, 16, 1024, ptx::kLayoutSw128), kIdQK,
+                         kk > 0);
+        }
+        ptx::umma_commit(&gb[kSFull + b]);
+        ptx::umma_commit(&bars[kKEmpty + kslot]);
+        if (r.j == r.nt - 1) ptx::umma_commit(&gb[kQEmpty]);
+      }
+      // nothing may be in flight when tensor memory is freed
+      ptx::umma_commit(&bars[kDrainQK]);
+      bool drain_aborted = false;
+      wait(&bars[kDrainQK], 0, drain_aborted);
+      if (aborted || drain_aborted) flags[0] = 1;
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ============================ P.V issue ============================
+    // Lane 0 waits and issues; the whole warp zeroes, in a tile whose last
+    // 16-token step is partly past the end of the sequence, the V rows past
+    // the end (they may hold stale or uninitialised data and P is 0 there).
+    // V tiles are consumed strictly in order, so the wait on the V ring is
+    // always for the phase after the one this warp consumed last.
+    constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, NP, 1, 1);
+    Stream st;
+    st.init(ctx, read_item, NoOp{});
+    Rec r;
+    while (!aborted && st.next(ctx, r, read_item, NoOp{})) {
+      uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
+      const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
+      const int vslot = static_cast<int>(r.u % NSV);
+      unsigned char* vt = vring + vslot * kUmmaTileBytes;
+      if (lane == 0) {
+        wait(&bars[kVFull + vslot], (r.u / NSV) & 1u, aborted);
+        wait(&gb[kPFull + b], ph, aborted);
+        wait(&gb[kOEmpty + b], ph ^ 1u, aborted);
+      }
+      aborted = __shfl_sync(0xffffffffu, aborted, 0);
+      if (aborted) break;
+      const int nks = (r.nv + 15) / 16;
+      if (r.nv & 15) {
+        const int row0 = r.nv, nrows = nks * 16 - r.nv;   // 1..15 rows, both halves
+        for (int c = lane; c < nrows * 16; c += 32) {
+          const int rr = row0 + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+          *reinterpret_cast<uint4*>(vt + half * 16384 + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+        ptx::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tc_fence_after();
+        const unsigned char* pt = pbuf + (r.g * 2 + b) * PB;
+        const uint32_t od = tmem + 64 + (r.g * 2 + b) * NP;
         for (int ks = 0; ks < nks; ++ks)
-          ptx::umma_bf16(tmem + 32 + b * NP,
-                         ptx::smem_desc(vt + ks * 2048, 16384, 1024, ptx::kLayoutSw128),
+          ptx::umma_bf16(od, ptx::smem_desc(vt + ks * 2048, 16384, 1024, ptx::kLayoutSw128),
                          ptx::smem_desc(pt + ks * 2 * PGRP * 128, PGRP * 128, 128, ptx::kLayoutNone),
                          kIdPV, ks > 0);
-        ptx::umma_commit(&bars[kOFull + b]);
-        ptx::umma_commit(&bars[kEmpty + vslot]);
-        ptx::umma_commit(&bars[kPEmpty + b]);
-      };
-      uint32_t u = 0, qi = 0;
-      for (int w = blockIdx.x; w < total && !aborted; w += gridDim.x) {
-        const Item it = item_at(p, prefix, w);
-        if (it.ntok <= 0) continue;
-        const int nt = (it.ntok + kUmmaTile - 1) / kUmmaTile;
-        const uint32_t qs = qi & 1u;
-        wait(&bars[kQFull + qs], (qi >> 1) & 1u, aborted);
-        const unsigned char* qt = qbuf + qs * kUmmaQBytes;
-        for (int j = 0; j < nt && !aborted; ++j, ++u) {
-          const uint32_t e = 2u * u;
-          const int kslot = static_cast<int>(e % NS);
-          const uint32_t b = u & 1u;
-          wait(&bars[kFull + kslot], (e / NS) & 1u, aborted);
-          wait(&bars[kSEmpty + b], ((u >> 1) & 1u) ^ 1u, aborted);
-          ptx::tc_fence_after();
-          const unsigned char* kt = ring + kslot * kUmmaTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int h = kk >> 2, k4 = kk & 3;
-            ptx::umma_bf16(tmem + b * 16,
-                           ptx::smem_desc(kt + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
-                           ptx::smem_desc(qt + h * 2048 + k4 * 32, 16, 1024, ptx::kLayoutSw128), kIdQK,
-                           kk > 0);
-          }
-          ptx::umma_commit(&bars[kSFull + b]);
-          ptx::umma_commit(&bars[kEmpty + kslot]);
-          if (j == nt - 1) ptx::umma_commit(&bars[kQEmpty + qs]);
-          if (have_prev) issue_pv(prev_u, prev_nv);
-          have_prev = true;
-          prev_u = u;
-          prev_nv = min(kUmmaTile, it.ntok - j * kUmmaTile);
-        }
-        ++qi;
+        ptx::umma_commit(&gb[kOFull + b]);
+        ptx::umma_commit(&bars[kVEmpty + vslot]);
+        ptx::umma_commit(&gb[kPEmpty + b]);
       }
-      if (have_prev && !aborted) issue_pv(prev_u, prev_nv);
-      // nothing may be in flight when tensor memory is freed
-      ptx::umma_commit(&bars[kDrain]);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      ptx::umma_commit(&bars[kDrainPV]);
       bool drain_aborted = false;
-      wait(&bars[kDrain], 0, drain_aborted);
+      wait(&bars[kDrainPV], 0, drain_aborted);
       if (aborted || drain_aborted) flags[0] = 1;
     }
     __syncwarp();
   } else {
-    // ===================== softmax, accumulation, epilogue =====================
-    const int ctid = tid - 64;
-    const int cw = warp - 2;                // compute warp 0..3
-    const int quarter = warp & 3;           // tensor-memory lanes 32*quarter .. +31
-    const int r = 32 * quarter + lane;      // token row of S, head-dim row of O
+    // ===================== compute groups: softmax, accumulate, epilogue =====================
+    const int cg = (warp - 2) >> 2;          // compute group 0 / 1
+    const int cw = (warp - 2) & 3;           // warp within the group
+    const int ctid = tid - 64 - 128 * cg;    // 0..127 within the group
+    const int quarter = warp & 3;            // tensor-memory lanes 32*quarter .. +31
+    const int r = 32 * quarter + lane;       // token row of S, head-dim row of O
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const uint32_t bar_id = 1 + cg;
     const float sl2 = p.scale_log2;
+    uint64_t* gb = bars + kGroup0 + cg * kUmmaGroupBars;
+    unsigned char* gp = pbuf + cg * 2 * PB;
+    float* red_m = reinterpret_cast<float*>(small + cg * kUmmaSmallBytes);  // [2][4][16]
+    float* red_l = red_m + 2 * 4 * 16;                                      // [4][16]
+    float* alpha_s = red_l + 4 * 16;                                        // [2][16]
+    volatile int* merge_flag = flags + 1 + cg;
+    volatile int* gabort = flags + 3 + cg;
 
     float m_run[G], l_thr[G], o_acc[G];
     float m_fin0[G], l_fin0[G], m_fin1[G], l_fin1[G];
@@ -315,14 +603,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       m_fin0[g] = m_fin1[g] = -CUDART_INF_F;
       l_fin0[g] = l_fin1[g] = 0.f;
     }
-    struct Prev {
-      uint32_t u;
-      int first, last, seq, kvh, part, nparts;
-    } prev = {0, 0, 0, 0, 0, 0, 0};
-    bool have_prev = false;
 
-    auto softmax = [&](uint32_t u, int nv, bool first, bool last) {
-      const uint32_t b = u & 1u, ph = (u >> 1) & 1u;
+    auto write_zeros = [&](int g_owner, const Item& it) {
+      if (g_owner != cg) return;  // the owning group writes the zero output
+      const int64_t ob = (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * HD + r;
+#pragma unroll
+      for (int g = 0; g < G; ++g) decode_detail::store_out(p.out, p.out_bf16, ob + g * HD, 0.f);
+    };
+
+    auto softmax = [&](const Rec& t) {
+      const uint32_t b = t.ug & 1u, ph = (t.ug >> 1) & 1u;
+      const bool first = t.j == 0, last = t.j == t.nt - 1;
       if (first) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -330,15 +621,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           l_thr[g] = 0.f;
         }
       }
-      wait(&bars[kSFull + b], ph, aborted);
+      wait(&gb[kSFull + b], ph, aborted);
       ptx::tc_fence_after();
       uint32_t sr[G];
-      ptx::TmemLd<G>::run(tmem + lane_base + b * 16, sr);
+      ptx::TmemLd<G>::run(tmem + lane_base + (cg * 2 + b) * 16, sr);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars[kSEmpty + b]);
-      const bool valid = r < nv;
+      if (lane == 0) ptx::mbar_arrive(&gb[kSEmpty + b]);
+      const bool valid = r < t.nv;
       float s[G], mx[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -353,7 +644,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
         for (int g = 0; g < G; ++g) red_m[(b * 4 + cw) * 16 + g] = mx[g];
       }
-      ptx::bar_sync(1, 128);
+      ptx::bar_sync(bar_id, 128);
       float pr[G], al[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -384,47 +675,35 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       }
       // P row r: columns [0, LO) hold bf16(p) of heads 0..G-1, columns
       // [LO, NP) the bf16 remainder p - bf16(p); unused heads are zero
-      float ph_[NP];
+      float pc[NP];
 #pragma unroll
-      for (int c = 0; c < NP; ++c) ph_[c] = 0.f;
+      for (int c = 0; c < NP; ++c) pc[c] = 0.f;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float hi = __bfloat162float(__float2bfloat16_rn(pr[g]));
-        ph_[g] = hi;
-        ph_[LO + g] = pr[g] - hi;
+        pc[g] = hi;
+        pc[LO + g] = pr[g] - hi;
       }
       uint32_t wp[NP / 2];
 #pragma unroll
-      for (int k = 0; k < NP / 2; ++k) wp[k] = pack_bf16(ph_[2 * k], ph_[2 * k + 1]);
-      wait(&bars[kPEmpty + b], ph ^ 1u, aborted);
-      unsigned char* prow = pbuf + b * kUmmaPBytes + (r >> 3) * (PGRP * 128) + (r & 7) * 16;
+      for (int k = 0; k < NP / 2; ++k) wp[k] = pack_bf16(pc[2 * k], pc[2 * k + 1]);
+      wait(&gb[kPEmpty + b], ph ^ 1u, aborted);
+      unsigned char* prow = gp + b * PB + (r >> 3) * (PGRP * 128) + (r & 7) * 16;
 #pragma unroll
       for (int c = 0; c < PGRP; ++c)
         *reinterpret_cast<uint4*>(prow + c * 128) =
             make_uint4(wp[4 * c], wp[4 * c + 1], wp[4 * c + 2], wp[4 * c + 3]);
-      if ((nv & 15) && r >= nv && r < ((nv + 15) & ~15)) {
-        // V rows past the end inside the last MMA step: zero them
-        const uint32_t e = 2u * u + 1u;
-        const int vslot = static_cast<int>(e % NS);
-        wait(&bars[kFull + vslot], (e / NS) & 1u, aborted);
-        unsigned char* vrow = ring + vslot * kUmmaTileBytes + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vrow + 16384 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars[kPFull + b]);
+      if (lane == 0) ptx::mbar_arrive(&gb[kPFull + b]);
     };
 
-    auto epilogue = [&](const Prev& t) {
+    auto epilogue = [&](const Rec& t) {
       float mf[G], lf[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        mf[g] = (t.u & 1u) ? m_fin1[g] : m_fin0[g];
-        lf[g] = (t.u & 1u) ? l_fin1[g] : l_fin0[g];
+        mf[g] = (t.ug & 1u) ? m_fin1[g] : m_fin0[g];
+        lf[g] = (t.ug & 1u) ? l_fin1[g] : l_fin0[g];
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
@@ -434,18 +713,19 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
         for (int g = 0; g < G; ++g) red_l[cw * 16 + g] = lf[g];
       }
-      ptx::bar_sync(1, 128);
+      ptx::bar_sync(bar_id, 128);
       float L[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) L[g] = red_l[g] + red_l[16 + g] + red_l[32 + g] + red_l[48 + g];
-      const int64_t obase = (static_cast<int64_t>(t.seq) * p.num_q_heads + t.kvh * G) * HD + r;
-      if (t.nparts == 1) {
+      const int64_t obase = (static_cast<int64_t>(t.it.seq) * p.num_q_heads + t.it.kvh * G) * HD + r;
+      if (t.it.nparts == 1) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, o_acc[g] / L[g]);
+        for (int g = 0; g < G; ++g)
+          decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, o_acc[g] / L[g]);
         return;
       }
-      const int row = t.seq * hkv + t.kvh;
-      const int64_t rec = static_cast<int64_t>(row) * p.max_parts + t.part;
+      const int row = t.it.seq * hkv + t.it.kvh;
+      const int64_t rec = static_cast<int64_t>(row) * p.max_parts + t.it.part;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         p.ws_o[(rec * G + g) * HD + r] = o_acc[g];
@@ -454,73 +734,101 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           p.ws_ml[rec * G * 2 + 2 * g + 1] = L[g];
         }
       }
-      ptx::bar_sync(1, 128);
+      // release: every writer orders its partial stores before the barrier;
+      // the counting thread acquires right after the atomic and only then
+      // publishes the result to the group
+      __threadfence();
+      ptx::bar_sync(bar_id, 128);
       if (ctid == 0) {
+        const int arrived = atomicAdd(&p.ws_counters[row], 1);
         __threadfence();
-        flags[1] = (atomicAdd(&p.ws_counters[row], 1) == t.nparts - 1) ? 1 : 0;
+        *merge_flag = (arrived == t.it.nparts - 1) ? 1 : 0;
       }
-      ptx::bar_sync(1, 128);
-      if (flags[1]) {
-        // last partition of this (sequence, kv head) to finish: merge
-        __threadfence();
+      ptx::bar_sync(bar_id, 128);
+      if (*merge_flag) {
+        // last partition of this (sequence, kv head) to finish: merge all
+        // heads at once so the partial loads are independent
         const float* ml = p.ws_ml + static_cast<int64_t>(row) * p.max_parts * G * 2;
         const float* os = p.ws_o + static_cast<int64_t>(row) * p.max_parts * G * HD + r;
-#pragma unroll 1
+        const int np = t.it.nparts;
+        float M[G], Ls[G], Os[G];
+#pragma unroll
         for (int g = 0; g < G; ++g) {
-          float M = -CUDART_INF_F;
-          for (int q = 0; q < t.nparts; ++q) M = fmaxf(M, __ldcg(ml + q * G * 2 + 2 * g));
-          float Ls = 0.f, Os = 0.f;
-          for (int q = 0; q < t.nparts; ++q) {
-            const float wq = exp2f(__ldcg(ml + q * G * 2 + 2 * g) - M);
-            Ls += wq * __ldcg(ml + q * G * 2 + 2 * g + 1);
-            Os += wq * __ldcg(os + (static_cast<int64_t>(q) * G + g) * HD);
-          }
-          decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, Os / Ls);
+          M[g] = -CUDART_INF_F;
+          Ls[g] = 0.f;
+          Os[g] = 0.f;
         }
+#pragma unroll 4
+        for (int q = 0; q < np; ++q)
+#pragma unroll
+          for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], __ldcg(ml + q * G * 2 + 2 * g));
+#pragma unroll 2
+        for (int q = 0; q < np; ++q) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float2 mlq = __ldcg(reinterpret_cast<const float2*>(ml + q * G * 2 + 2 * g));
+            const float wq = exp2f(mlq.x - M[g]);
+            Ls[g] = fmaf(wq, mlq.y, Ls[g]);
+            Os[g] = fmaf(wq, __ldcg(os + (static_cast<int64_t>(q) * G + g) * HD), Os[g]);
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, Os[g] / Ls[g]);
         if (ctid == 0) p.ws_counters[row] = 0;
       }
     };
 
-    auto accumulate = [&](const Prev& t) {
-      const uint32_t b = t.u & 1u, ph = (t.u >> 1) & 1u;
-      wait(&bars[kOFull + b], ph, aborted);
+    auto accumulate = [&](const Rec& t) {
+      const uint32_t b = t.ug & 1u, ph = (t.ug >> 1) & 1u;
+      wait(&gb[kOFull + b], ph, aborted);
       ptx::tc_fence_after();
       uint32_t orr[NP];
-      ptx::TmemLd<NP>::run(tmem + lane_base + 32 + b * NP, orr);
+      ptx::TmemLd<NP>::run(tmem + lane_base + 64 + (cg * 2 + b) * NP, orr);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty + b]);
+      if (lane == 0) ptx::mbar_arrive(&gb[kOEmpty + b]);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float o = __uint_as_float(orr[g]) + __uint_as_float(orr[LO + g]);
-        o_acc[g] = t.first ? o : fmaf(o_acc[g], alpha_s[b * 16 + g], o);
+        o_acc[g] = t.j == 0 ? o : fmaf(o_acc[g], alpha_s[b * 16 + g], o);
       }
-      if (t.last) epilogue(t);
+      if (t.j == t.nt - 1) epilogue(t);
     };
 
-    uint32_t u = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      const Item it = item_at(p, prefix, w);
-      if (it.ntok <= 0) {  // empty sequence: zero output
-        const int64_t obase = (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * HD + r;
-#pragma unroll
-        for (int g = 0; g < G; ++g) decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, 0.f);
-        continue;
+    // this group's items only, in queue order
+    GroupIter gi;
+    gi.k = gi.items = 0;
+    seek(ctx, gi, cg, read_item, write_zeros);
+    uint32_t ug = 0;
+    Rec t, prev;
+    bool have_prev = false;
+    while (gi.valid) {
+      t.g = cg;
+      t.it = gi.it;
+      t.j = gi.j;
+      t.nt = gi.nt;
+      t.nv = min(kUmmaTile, gi.it.ntok - gi.j * kUmmaTile);
+      t.u = 0;
+      t.ug = ug++;
+      t.qi = gi.items;
+      if (++gi.j == gi.nt) {
+        ++gi.items;
+        seek(ctx, gi, cg, read_item, write_zeros);
       }
-      const int nt = (it.ntok + kUmmaTile - 1) / kUmmaTile;
-      for (int j = 0; j < nt; ++j, ++u) {
-        const int nv = min(kUmmaTile, it.ntok - j * kUmmaTile);
-        softmax(u, nv, j == 0, j == nt - 1);
-        if (have_prev) accumulate(prev);
-        prev = Prev{u, j == 0, j == nt - 1, it.seq, it.kvh, it.part, it.nparts};
-        have_prev = true;
+      softmax(t);
+      if (have_prev) accumulate(prev);
+      prev = t;
+      have_prev = true;
+      if (t.j == t.nt - 1) {
+        // item boundary: the group leaves together if any thread gave up
+        if (aborted) *gabort = 1;
+        ptx::bar_sync(bar_id, 128);
+        if (*gabort) break;  // uniform: read after the barrier, written only before one
       }
-      if (aborted) flags[2] = 1;
-      ptx::bar_sync(1, 128);
-      if (flags[2]) break;  // uniform: read after the barrier, written only before one
     }
-    if (have_prev && !flags[2]) accumulate(prev);
+    ptx::bar_sync(bar_id, 128);
+    if (have_prev && !*gabort) accumulate(prev);
   }
 
   // ============================ teardown ============================
@@ -529,7 +837,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
-  if (tid == 0 && (flags[0] || flags[2])) atomicExch(p.ws_err, kDevErrTimeout);
+  if (tid == 0) {
+    if (flags[0] || flags[3] || flags[4]) atomicExch(p.ws_err, kDevErrTimeout);
+    // the last CTA to finish returns the item counter to zero for the next call
+    __threadfence();
+    if (atomicAdd(done_counter, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(item_counter, 0);
+      atomicExch(done_counter, 0);
+    }
+  }
 }
 
 }  // namespace pa

@@ -140,3 +140,20 @@ def test_workspace_too_small_is_rejected(ops):
         ops.pa_decode(out, g.q, g.k_cache, g.v_cache, g.tables, g.lens, wl.scale, 2, 600, ws,
                       partition_tokens=64)
     assert e.value.status == 5
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 512, 2048])
+def test_batch256_repeated_calls_bit_identical(ops, partition_tokens):
+    """Repeated decodes of the batch-256 workload on one reused workspace give
+    identical bits (the split-K merge order and every tile's arithmetic are
+    fixed by logical position), and agree with the oracle."""
+    wl = W.gqa_bf16()
+    g = GpuState(wl, ops)
+    ws = ops.make_workspace(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                            wl.block_size, wl.dtype, g.max_len, partition_tokens)
+    first = g.decode(partition_tokens=partition_tokens, workspace=ws)
+    for _ in range(12):
+        assert torch.equal(g.decode(partition_tokens=partition_tokens, workspace=ws), first)
+    rows = sample_seqs(wl.context_lens, 16, seed=partition_tokens + 3)
+    ref = OracleState(wl, seqs=rows).decode(seqs=rows)
+    assert max_err(first, ref, rows) <= TOL["bf16"]
