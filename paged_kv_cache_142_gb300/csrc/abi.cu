@@ -135,7 +135,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
       off += 4 * tbl_stride * 4;
       pl->off_lens = static_cast<int>(off);
       off += round_up(static_cast<int64_t>(num_seqs) * 4, 16);
-      pl->off_prefix = static_cast<int>(off);  // two prefix arrays of (num_seqs + 4) & ~3 ints
+      pl->off_prefix = static_cast<int>(off);  // prefix and tail-order arrays of (num_seqs + 4) & ~3 ints
       off += 2 * round_up((static_cast<int64_t>(num_seqs) + 4) / 4 * 4 * 4, 16);
       pl->smem = static_cast<int>(off + 1024);  // slack to align the base to 1024 bytes
     }
@@ -203,6 +203,23 @@ bool encode_rows_128(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D map over the K or V pool viewed as 8-row groups: (64 dims of a
+// 128-byte swizzle span, 8 rows 256 bytes apart, 2 halves of the row 128
+// bytes apart, row groups 2048 bytes apart).  One box of box_rows rows lands
+// in shared memory as [row group][half][8 rows][128 B]: every 8-row atom of
+// a half is a 1024-byte swizzle atom, atoms of one half 2048 bytes apart.
+bool encode_kv_groups(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, 8, 2, static_cast<cuuint64_t>(rows / 8)};
+  cuuint64_t strides[3] = {256, 128, 2048};
+  cuuint32_t box[4] = {64, 8, 2, box_rows / 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -401,15 +418,16 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
 
   cudaError_t e;
   if (pl.umma) {
-    // TMA tensor maps over the K and V pools (rows of 128 dims, one box per
-    // block and 64-dim half) and over the queries (one box per GQA group)
+    // TMA tensor maps over the K and V pools (one box per block, at most 128
+    // rows, in 8-row groups) and over the queries (one box per GQA group and
+    // 64-dim half)
     const int64_t cache_rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     const int64_t q_rows = static_cast<int64_t>(num_seqs) * num_q_heads;
     if (cache_rows >= (int64_t(1) << 31) || q_rows >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
     CUtensorMap tmk, tmv, tmq;
     const uint32_t box_rows = static_cast<uint32_t>(block_size < 128 ? block_size : 128);
-    if (!encode_rows_128(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
-        !encode_rows_128(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
+    if (!encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
+        !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
         !encode_rows_128(&tmq, q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(pl.group)))
       return PA_ERR_CUDA;
     void* args[] = {&p, &tmk, &tmv, &tmq};

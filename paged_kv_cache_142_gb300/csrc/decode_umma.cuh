@@ -15,20 +15,21 @@
 //
 // One CTA per SM, persistent over (sequence, kv head, partition) work items.
 // Items are enumerated from context_lens in shared memory, full partitions
-// first and the shorter last partitions after them, and claimed
+// first and the shorter last partitions after them, longest first, and claimed
 // dynamically: the K-stream warp takes the next item index from a global
-// counter in the workspace whenever one of the CTA's two compute groups
-// needs work, and publishes it to that group's queue in shared memory,
+// counter in the workspace when one of the CTA's two compute groups reaches
+// the last tile of its item, and publishes it to that group's queue in shared memory,
 // which every other role reads in order.  The two groups' 128-token tiles
 // are interleaved into one stream (group 0 tile, group 1 tile, ...) that
 // every stream-walking warp derives identically.  The K path and the V path run decoupled,
 // each with its own ring of 32 KB stages, streaming warp and MMA warp:
-//  * warp 0 streams K: per item it hoists the partition's block-table slice
-//    into shared memory (cp.async, issued as soon as the item is known, into
-//    a double-buffered slice) and loads the query rows (TMA tensor copy);
-//    per tile
-//    it issues, from one lane per block, TMA tensor copies (128-byte swizzle,
-//    L2 evict-first) of that block's K rows into the K ring;
+//  * warp 0 streams K: per item it copies the partition's block-table slice
+//    into shared memory and loads the query rows (TMA tensor copy); per tile
+//    it issues, from one lane per block, one 4-D TMA tensor copy (128-byte
+//    swizzle, L2 evict-first) of that block's K rows into the K ring, laid
+//    out as [8-row group][64-dim half][8 rows][128 B] so that each 8-row
+//    half is one swizzle atom of the K-major (Q.K^T) and MN-major (P.V)
+//    operands;
 //  * warp 10 streams V the same way into the V ring;
 //  * warp 1 owns the tensor memory (per group: S and O, double-buffered) and
 //    one lane issues Q.K^T of every tile as soon as its K tile has landed;
@@ -60,7 +61,7 @@ namespace pa {
 
 constexpr int kUmmaThreads = 384;        // 0 K stream, 1 Q.K MMA, 2-9 compute, 10 V stream, 11 P.V MMA
 constexpr int kUmmaTile = 128;           // tokens per tile (MMA M)
-constexpr int kUmmaTileBytes = 32768;    // one K or V tile: 2 halves x 128 rows x 128 B
+constexpr int kUmmaTileBytes = 32768;    // one K or V tile: 16 row groups x 2 halves x 8 rows x 128 B
 constexpr int kUmmaMaxStages = 8;
 constexpr int kUmmaQBytes = 4096;        // query tile: 2 halves x 16 rows x 128 B (one per group)
 constexpr int kUmmaSmallBytes = 1024;    // per group: reductions and rescale factors
@@ -92,14 +93,20 @@ struct Item {
 };
 
 // Item enumeration: first every full partition (part_tokens tokens) of
-// every sequence, sequence-major, kv head fastest; then every sequence's
-// last, shorter partition (or its single empty item when len == 0).
-// prefix_full / prefix_tail hold the exclusive prefix sums of the per
-// sequence item counts of the two phases.
+// every sequence, sequence-major, kv head fastest; then the sequences' last,
+// shorter partitions (a sequence of length 0: one empty item per kv head),
+// longest first: by 128-token tile count (counts of kTailBuckets - 1 and
+// more share one class), sequence order within a count, empty ones last; kv
+// head fastest.  Every CTA derives the same order from context_lens, so an
+// item index names the same work in every CTA; handing out the long work
+// first leaves short items for the end of the launch, where they even out
+// the CTAs' finishing times.
+constexpr int kTailBuckets = 64;
+
 struct Ctx {
   const DecodeParams* p;
-  const int32_t* prefix_full;
-  const int32_t* prefix_tail;
+  const int32_t* prefix_full;  // exclusive prefix of the full-partition item counts
+  const int32_t* tail_seq;     // sequences with a last partition, in item order
   const int32_t* lens;
   int n_full, total;
 };
@@ -126,8 +133,9 @@ __device__ __forceinline__ Item item_at(const Ctx& c, int w) {
     it.kvh = u - it.part * hkv;
   } else {
     const int v = w - c.n_full;
-    it.seq = seq_of(v, c.prefix_tail, c.p->num_seqs);
-    it.kvh = v - c.prefix_tail[it.seq];
+    const int sp = v / hkv;
+    it.seq = c.tail_seq[sp];
+    it.kvh = v - sp * hkv;
     it.part = c.lens[it.seq] / pt;
   }
   it.len = c.lens[it.seq];
@@ -137,58 +145,91 @@ __device__ __forceinline__ Item item_at(const Ctx& c, int w) {
   return it;
 }
 
-// Builds lens, prefix_full and prefix_tail; every thread calls it; the CTA
-// is synchronised on return.  CTA 0 reports lengths outside
-// [0, max_context_len] in the workspace error word.
-__device__ __forceinline__ void build_two_phase_prefix(const DecodeParams& p, int32_t* lens,
-                                                       int32_t* prefix_full, int32_t* prefix_tail,
-                                                       int* warp_sums, int tid, int nthreads) {
+// Class of a sequence's last partition: -1 none (length a positive multiple
+// of the partition), 0 empty sequence, else its 128-token tile count capped.
+__device__ __forceinline__ int tail_class(int len, int pt) {
+  if (len == 0) return 0;
+  const int r = len % pt;
+  if (r == 0) return -1;
+  return min((r + kUmmaTile - 1) / kUmmaTile, kTailBuckets - 1);
+}
+
+// Builds lens, prefix_full and tail_seq and returns the number of sequences
+// with a last partition; every thread calls it; the CTA is synchronised on
+// return.  hist: kTailBuckets + 1 ints of scratch.  CTA 0 reports lengths
+// outside [0, max_context_len] in the workspace error word.
+__device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* lens,
+                                                int32_t* prefix_full, int32_t* tail_seq,
+                                                int* warp_sums, int* hist, int tid, int nthreads) {
   const int nseq = p.num_seqs, pt = p.part_tokens, hkv = p.num_kv_heads;
-  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  const int lane = tid & 31, warp = tid >> 5;
   const int per = (nseq + nthreads - 1) / nthreads;
   const int beg = min(nseq, tid * per);
   const int end = min(nseq, beg + per);
-  int lf = 0, lt = 0;
+  if (tid < kTailBuckets) hist[tid] = 0;
+  __syncthreads();
+  int lf = 0;
   for (int i = beg; i < end; ++i) {
     const int raw = p.context_lens[i];
     if (blockIdx.x == 0 && (raw < 0 || raw > p.max_context_len)) atomicExch(p.ws_err, kDevErrInvalidArg);
     const int len = decode_detail::clamp_len(raw, p.max_context_len);
     lens[i] = len;
     lf += (len / pt) * hkv;
-    lt += (len % pt != 0 || len == 0) ? hkv : 0;
+    const int c = tail_class(len, pt);
+    if (c >= 0) atomicAdd(&hist[c], 1);
   }
-  int xf = lf, xt = lt;
+  int xf = lf;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int yf = __shfl_up_sync(0xffffffffu, xf, off);
-    const int yt = __shfl_up_sync(0xffffffffu, xt, off);
-    if (lane >= off) {
-      xf += yf;
-      xt += yt;
-    }
+    if (lane >= off) xf += yf;
   }
-  if (lane == 31) {
-    warp_sums[warp] = xf;
-    warp_sums[nwarps + warp] = xt;
-  }
+  if (lane == 31) warp_sums[warp] = xf;
   __syncthreads();
-  int rf = xf - lf, rt = xt - lt;
-  for (int w = 0; w < warp; ++w) {
-    rf += warp_sums[w];
-    rt += warp_sums[nwarps + w];
-  }
+  int rf = xf - lf;
+  for (int w = 0; w < warp; ++w) rf += warp_sums[w];
   for (int i = beg; i < end; ++i) {
-    const int len = lens[i];
     prefix_full[i] = rf;
-    prefix_tail[i] = rt;
-    rf += (len / pt) * hkv;
-    rt += (len % pt != 0 || len == 0) ? hkv : 0;
+    rf += (lens[i] / pt) * hkv;
   }
-  if (tid == nthreads - 1) {
-    prefix_full[nseq] = rf;
-    prefix_tail[nseq] = rt;
+  if (tid == nthreads - 1) prefix_full[nseq] = rf;
+  __syncthreads();
+  if (warp == 0) {
+    // class bases, longest class first: lane l owns classes 63 - 2l and 62 - 2l
+    static_assert(kTailBuckets == 64, "two classes per lane");
+    const int c0 = hist[kTailBuckets - 1 - 2 * lane], c1 = hist[kTailBuckets - 2 - 2 * lane];
+    int x = c0 + c1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, x, 31);
+    const int ex = x - c0 - c1;
+    __syncwarp();
+    hist[kTailBuckets - 1 - 2 * lane] = ex;
+    hist[kTailBuckets - 2 - 2 * lane] = ex + c0;
+    __syncwarp();
+    // stable placement, 32 sequences at a time
+    for (int c = 0; c < nseq; c += 32) {
+      const int s = c + lane;
+      const int k = s < nseq ? tail_class(lens[s], pt) : -1;
+      const unsigned m = __match_any_sync(0xffffffffu, k);
+      const int rank = __popc(m & ((1u << lane) - 1u));
+      const int pos = k >= 0 ? hist[k] + rank : 0;
+      __syncwarp();
+      if (k >= 0) {
+        tail_seq[pos] = s;
+        if (rank == 0) hist[k] += __popc(m);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) hist[kTailBuckets] = total;
   }
   __syncthreads();
+  const int n_tail = hist[kTailBuckets];
+  __syncthreads();  // hist is shared scratch of later roles
+  return n_tail;
 }
 
 // One compute group's item sequence, as published in its queue.
@@ -328,7 +369,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   int32_t* tbl = reinterpret_cast<int32_t*>(smem + p.off_tbl);  // [K/V stream][group][tbl_stride]
   int32_t* lens = reinterpret_cast<int32_t*>(smem + p.off_lens);
   int32_t* prefix_full = reinterpret_cast<int32_t*>(smem + p.off_prefix);
-  int32_t* prefix_tail = prefix_full + ((p.num_seqs + 4) & ~3);
+  int32_t* tail_seq = prefix_full + ((p.num_seqs + 4) & ~3);
   volatile int* queue = reinterpret_cast<volatile int*>(small + 2 * kUmmaSmallBytes);  // [group][kUmmaQueue]
 
   const int tid = threadIdx.x;
@@ -372,11 +413,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     ptx::tmem_alloc(tmem_slot, TMEM_COLS);
     ptx::tc_fence_before();
   }
-  build_two_phase_prefix(p, lens, prefix_full, prefix_tail, warp_sums, tid, kUmmaThreads);  // syncs
+  const int n_tail = build_item_order(p, lens, prefix_full, tail_seq, warp_sums,
+                                      reinterpret_cast<int*>(small), tid, kUmmaThreads);  // syncs
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_full = prefix_full[p.num_seqs];
-  const Ctx ctx{&p, prefix_full, prefix_tail, lens, n_full, n_full + prefix_tail[p.num_seqs]};
+  const Ctx ctx{&p, prefix_full, tail_seq, lens, n_full, n_full + n_tail * p.num_kv_heads};
   bool aborted = false;
   int* item_counter = p.ws_err + 1;   // next unclaimed item (all CTAs)
   int* done_counter = p.ws_err + 2;   // CTAs finished
@@ -410,9 +452,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     uint64_t* empty = bars + (is_v ? kVEmpty : kKEmpty);
     const int NS = is_v ? NSV : NSK;
     const int box_rows = min(bs, kUmmaTile);
+    const int bs_log = __ffs(bs) - 1;  // block size is a power of two
     // warp 0 claims items for both groups and publishes them; warp 10 reads.
-    // A claim is made only when a group needs its next item, so no CTA
-    // holds work another could start sooner.
+    // A claim is made only when the stream takes a group's last tile of its
+    // current item, so no CTA holds work another could start sooner.
     auto publish_item = [&](int g, uint32_t k) -> int {
       int w = -1;
       if (lane == 0) {
@@ -432,12 +475,14 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     auto slice = [&](int g) -> int32_t* { return tbl + ((is_v ? 2 : 0) + g) * p.tbl_stride; };
     Stream st;
     st.init(ctx, next_w, NoOp{});
+    int slot = 0;
+    uint32_t phase = 0;
     Rec r;
     while (!aborted && st.next(ctx, r, next_w, NoOp{})) {
       int32_t* gtbl = slice(r.g);
-      const int b0 = r.it.t0 / bs;
+      const int b0 = r.it.t0 >> bs_log;
       if (r.j == 0) {
-        const int nb = (r.it.t0 + r.it.ntok + bs - 1) / bs - b0;
+        const int nb = ((r.it.t0 + r.it.ntok + bs - 1) >> bs_log) - b0;
         const int32_t* trow = p.block_tables + static_cast<int64_t>(r.it.seq) * p.max_blocks_per_seq + b0;
         for (int j = lane; j < nb; j += 32) gtbl[j] = trow[j];
         __syncwarp();
@@ -457,26 +502,28 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       int row = 0;
       if (lane < nbox) {
         const int tok = tok0 + lane * box_rows;
-        const int lb = tok / bs;
+        const int lb = tok >> bs_log;
         int phys = gtbl[lb - b0];
         if (phys < 0 || phys >= p.num_blocks) {  // never read outside the pool
           atomicExch(p.ws_err, kDevErrInvalidArg);
           phys = 0;
         }
-        row = (phys * hkv + r.it.kvh) * bs + (tok - lb * bs);
+        row = ((phys * hkv + r.it.kvh) << bs_log) + (tok - (lb << bs_log));
       }
-      const int slot = static_cast<int>(r.u % NS);
       if (lane == 0) {
-        wait(&empty[slot], ((r.u / NS) & 1u) ^ 1u, aborted);
+        wait(&empty[slot], phase ^ 1u, aborted);
         ptx::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * box_rows * 256));
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
       if (!aborted && lane < nbox) {
-        unsigned char* dst = ring + slot * kUmmaTileBytes + lane * box_rows * 128;
-        ptx::tma_load_2d(dst, tm, 0, row, &full[slot], pol_kv);
-        ptx::tma_load_2d(dst + 16384, tm, 64, row, &full[slot], pol_kv);
+        unsigned char* dst = ring + slot * kUmmaTileBytes + lane * box_rows * 256;
+        ptx::tma_load_4d(dst, tm, 0, 0, 0, row >> 3, &full[slot], pol_kv);
       }
       __syncwarp();
+      if (++slot == NS) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
   } else if (warp == 1) {
     // ============================ Q.K^T issue ============================
@@ -492,12 +539,13 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       Stream st;
       st.init(ctx, read_one, NoOp{});
       Rec r;
+      int kslot = 0;
+      uint32_t kph = 0;
       while (!aborted && st.next(ctx, r, read_one, NoOp{})) {
         uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
         const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
         if (r.j == 0) wait(&gb[kQFull], r.qi & 1u, aborted);
-        const int kslot = static_cast<int>(r.u % NSK);
-        wait(&bars[kKFull + kslot], (r.u / NSK) & 1u, aborted);
+        wait(&bars[kKFull + kslot], kph, aborted);
         wait(&gb[kSEmpty + b], ph ^ 1u, aborted);
         ptx::tc_fence_after();
         const unsigned char* kt = kring + kslot * kUmmaTileBytes;
@@ -506,13 +554,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const int h = kk >> 2, k4 = kk & 3;
-          ptx::umma_bf16(sd, ptx::smem_desc(kt + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
+          ptx::umma_bf16(sd, ptx::smem_desc(kt + h * 1024 + k4 * 32, 16, 2048, ptx::kLayoutSw128),
                          ptx::smem_desc(qt + h * 2048 + k4 * 32, 16, 1024, ptx::kLayoutSw128), kIdQK,
                          kk > 0);
         }
         ptx::umma_commit(&gb[kSFull + b]);
         ptx::umma_commit(&bars[kKEmpty + kslot]);
         if (r.j == r.nt - 1) ptx::umma_commit(&gb[kQEmpty]);
+        if (++kslot == NSK) {
+          kslot = 0;
+          kph ^= 1u;
+        }
       }
       // nothing may be in flight when tensor memory is freed
       ptx::umma_commit(&bars[kDrainQK]);
@@ -532,13 +584,14 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     Stream st;
     st.init(ctx, read_item, NoOp{});
     Rec r;
+    int vslot = 0;
+    uint32_t vph = 0;
     while (!aborted && st.next(ctx, r, read_item, NoOp{})) {
       uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
       const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
-      const int vslot = static_cast<int>(r.u % NSV);
       unsigned char* vt = vring + vslot * kUmmaTileBytes;
       if (lane == 0) {
-        wait(&bars[kVFull + vslot], (r.u / NSV) & 1u, aborted);
+        wait(&bars[kVFull + vslot], vph, aborted);
         wait(&gb[kPFull + b], ph, aborted);
         wait(&gb[kOEmpty + b], ph ^ 1u, aborted);
       }
@@ -549,7 +602,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         const int row0 = r.nv, nrows = nks * 16 - r.nv;   // 1..15 rows, both halves
         for (int c = lane; c < nrows * 16; c += 32) {
           const int rr = row0 + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
-          *reinterpret_cast<uint4*>(vt + half * 16384 + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
         }
         ptx::fence_proxy_async_smem();
       }
@@ -559,7 +613,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         const unsigned char* pt = pbuf + (r.g * 2 + b) * PB;
         const uint32_t od = tmem + 64 + (r.g * 2 + b) * NP;
         for (int ks = 0; ks < nks; ++ks)
-          ptx::umma_bf16(od, ptx::smem_desc(vt + ks * 2048, 16384, 1024, ptx::kLayoutSw128),
+          ptx::umma_bf16(od, ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128),
                          ptx::smem_desc(pt + ks * 2 * PGRP * 128, PGRP * 128, 128, ptx::kLayoutNone),
                          kIdPV, ks > 0);
         ptx::umma_commit(&gb[kOFull + b]);
@@ -567,6 +621,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         ptx::umma_commit(&gb[kPEmpty + b]);
       }
       __syncwarp();
+      if (++vslot == NSV) {
+        vslot = 0;
+        vph ^= 1u;
+      }
     }
     if (lane == 0) {
       ptx::umma_commit(&bars[kDrainPV]);

@@ -119,6 +119,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tensor_m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tensor_map, int x, int y, int z,
+                                            int w, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst_smem)),
+      "l"(tensor_map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void* tensor_map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tensor_map) : "memory");
 }
