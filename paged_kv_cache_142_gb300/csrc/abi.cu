@@ -49,7 +49,7 @@ pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_
 }
 
 // Tensor-core kernel layout constants (must match decode_umma.cuh).
-constexpr int kUmmaThreadsHost = 384;
+constexpr int kUmmaThreadsHost = 448;
 constexpr int kUmmaTileBytesHost = 32768;
 
 struct Plan {

@@ -31,11 +31,16 @@
 //    half is one swizzle atom of the K-major (Q.K^T) and MN-major (P.V)
 //    operands;
 //  * warp 10 streams V the same way into the V ring;
-//  * warp 1 owns the tensor memory (per group: S and O, double-buffered) and
-//    one lane issues Q.K^T of every tile as soon as its K tile has landed;
-//  * warp 11 issues P.V of every tile once its V tile has landed and its P
-//    is ready (zeroing first the V rows past the end of a sequence inside
-//    the tile's last 16-token step);
+//  * warps 1 and 12 issue Q.K^T (one lane each) of group 0's and group 1's
+//    tiles as soon as the tile's K has landed; warp 1 owns the tensor memory
+//    (per group: S and O, double-buffered);
+//  * warps 11 and 13 issue P.V of group 0's and group 1's tiles once the
+//    tile's V has landed and its P is ready (zeroing first the V rows past
+//    the end of a sequence inside the tile's last 16-token step).  One
+//    issuing thread per group and product keeps a group's tile from waiting
+//    behind the other group's in one in-order issuer (an MMA takes a thread
+//    about a hundred cycles to issue whatever its size; separate warps
+//    issue in parallel);
 //  * warps 2-5 and 6-9 are the two compute groups (one thread per token row,
 //    then per head-dim row): online softmax in fp32 on the score tile (block
 //    max via shuffles + shared memory, exp2 in the log2 domain), P written to
@@ -59,7 +64,9 @@
 
 namespace pa {
 
-constexpr int kUmmaThreads = 384;        // 0 K stream, 1 Q.K MMA, 2-9 compute, 10 V stream, 11 P.V MMA
+// warps: 0 K stream, 1 / 12 Q.K^T MMA of group 0 / 1, 2-9 compute, 10 V
+// stream, 11 / 13 P.V MMA of group 0 / 1
+constexpr int kUmmaThreads = 448;
 constexpr int kUmmaTile = 128;           // tokens per tile (MMA M)
 constexpr int kUmmaTileBytes = 32768;    // one K or V tile: 16 row groups x 2 halves x 8 rows x 128 B
 constexpr int kUmmaMaxStages = 8;
@@ -67,25 +74,31 @@ constexpr int kUmmaQBytes = 4096;        // query tile: 2 halves x 16 rows x 128
 constexpr int kUmmaSmallBytes = 1024;    // per group: reductions and rescale factors
 constexpr int kUmmaGroupBars = 16;
 constexpr int kUmmaQueue = 8;            // per-group item queue depth
-constexpr int kUmmaQueueReaders = 7;     // V stream, Q.K warp, P.V warp, 4 compute warps
-constexpr int kUmmaBarriers = 4 * kUmmaMaxStages + 2 * kUmmaGroupBars + 2 + 4 * kUmmaQueue;
+constexpr int kUmmaQueueReaders = 9;     // V stream, 2 Q.K and 2 P.V warps, a group's 4 compute warps
+constexpr int kUmmaBarriers = 6 * kUmmaMaxStages + 2 * kUmmaGroupBars + 4 + 4 * kUmmaQueue;
 
 __host__ __device__ constexpr int umma_p_bytes(int G) { return G <= 8 ? 4096 : 8192; }
 
 namespace umma_detail {
 
-// barrier indices: K ring, V ring, per-group blocks, drains
-constexpr int kKFull = 0;
-constexpr int kKEmpty = kUmmaMaxStages;
-constexpr int kVFull = 2 * kUmmaMaxStages;
-constexpr int kVEmpty = 3 * kUmmaMaxStages;
-constexpr int kGroup0 = 4 * kUmmaMaxStages;
+// barrier indices: K ring, V ring, per-group blocks, drains.  A ring slot
+// has two "full" barriers that its successive fills use in turn: the two
+// groups' MMA warps consume the shared rings independently, and a consumer
+// waiting for fill k of a slot may find fill k - 1 not yet landed but never
+// fill k - 2 (its own previous tile was at most two tiles back, which forced
+// fill k - 1 to be issued, which needs fill k - 2 released), so a parity
+// wait on the copy used by fills k - 2, k, k + 2 cannot alias.
+constexpr int kKFull = 0;                          // [fill parity][stage]
+constexpr int kKEmpty = 2 * kUmmaMaxStages;
+constexpr int kVFull = 3 * kUmmaMaxStages;         // [fill parity][stage]
+constexpr int kVEmpty = 5 * kUmmaMaxStages;
+constexpr int kGroup0 = 6 * kUmmaMaxStages;
 // within a group's block of kUmmaGroupBars
 constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kSEmpty = 6, kPFull = 8, kPEmpty = 10,
               kOFull = 12, kOEmpty = 14;
-constexpr int kDrainQK = 4 * kUmmaMaxStages + 2 * kUmmaGroupBars;
-constexpr int kDrainPV = kDrainQK + 1;
-constexpr int kItemFull = kDrainPV + 1;                   // [group][kUmmaQueue]
+constexpr int kDrainQK = 6 * kUmmaMaxStages + 2 * kUmmaGroupBars;   // [group]
+constexpr int kDrainPV = kDrainQK + 2;                               // [group]
+constexpr int kItemFull = kDrainPV + 2;                   // [group][kUmmaQueue]
 constexpr int kItemEmpty = kItemFull + 2 * kUmmaQueue;    // [group][kUmmaQueue]
 
 struct Item {
@@ -365,7 +378,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   // [0] a streaming or MMA role gave up, [1..2] group merges its item,
   // [3..4] group gave up
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* warp_sums = const_cast<int*>(flags) + 5;   // 2 x 12 ints
+  int* warp_sums = const_cast<int*>(flags) + 5;   // one int per warp
   int32_t* tbl = reinterpret_cast<int32_t*>(smem + p.off_tbl);  // [K/V stream][group][tbl_stride]
   int32_t* lens = reinterpret_cast<int32_t*>(smem + p.off_lens);
   int32_t* prefix_full = reinterpret_cast<int32_t*>(smem + p.off_prefix);
@@ -381,10 +394,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < NSK; ++s) {
       ptx::mbar_init(&bars[kKFull + s], 1);
+      ptx::mbar_init(&bars[kKFull + kUmmaMaxStages + s], 1);
       ptx::mbar_init(&bars[kKEmpty + s], 1);
     }
     for (int s = 0; s < NSV; ++s) {
       ptx::mbar_init(&bars[kVFull + s], 1);
+      ptx::mbar_init(&bars[kVFull + kUmmaMaxStages + s], 1);
       ptx::mbar_init(&bars[kVEmpty + s], 1);
     }
     for (int g = 0; g < 2; ++g) {
@@ -400,8 +415,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         ptx::mbar_init(&gb[kOEmpty + b], 4);
       }
     }
-    ptx::mbar_init(&bars[kDrainQK], 1);
-    ptx::mbar_init(&bars[kDrainPV], 1);
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(&bars[kDrainQK + g], 1);
+      ptx::mbar_init(&bars[kDrainPV + g], 1);
+    }
     for (int q = 0; q < 2 * kUmmaQueue; ++q) {
       ptx::mbar_init(&bars[kItemFull + q], 1);
       ptx::mbar_init(&bars[kItemEmpty + q], kUmmaQueueReaders);
@@ -476,7 +493,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     Stream st;
     st.init(ctx, next_w, NoOp{});
     int slot = 0;
-    uint32_t phase = 0;
+    uint32_t wrap = 0;  // fills of each slot so far: full copy wrap & 1, empty parity
     Rec r;
     while (!aborted && st.next(ctx, r, next_w, NoOp{})) {
       int32_t* gtbl = slice(r.g);
@@ -510,23 +527,26 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         row = ((phys * hkv + r.it.kvh) << bs_log) + (tok - (lb << bs_log));
       }
+      uint64_t* fb = &full[(wrap & 1u) * kUmmaMaxStages + slot];
       if (lane == 0) {
-        wait(&empty[slot], phase ^ 1u, aborted);
-        ptx::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * box_rows * 256));
+        wait(&empty[slot], (wrap & 1u) ^ 1u, aborted);
+        ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nbox * box_rows * 256));
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
       if (!aborted && lane < nbox) {
         unsigned char* dst = ring + slot * kUmmaTileBytes + lane * box_rows * 256;
-        ptx::tma_load_4d(dst, tm, 0, 0, 0, row >> 3, &full[slot], pol_kv);
+        ptx::tma_load_4d(dst, tm, 0, 0, 0, row >> 3, fb, pol_kv);
       }
       __syncwarp();
       if (++slot == NS) {
         slot = 0;
-        phase ^= 1u;
+        ++wrap;
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 12) {
     // ============================ Q.K^T issue ============================
+    // warp 1: group 0's tiles (and the tensor memory), warp 12: group 1's
+    const int my_g = warp == 12 ? 1 : 0;
     if (lane == 0) {
       constexpr uint32_t kIdQK = ptx::idesc_bf16_f32(128, 16, 0, 0);
       auto read_one = [&](int g, uint32_t k) -> int {
@@ -540,12 +560,19 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       st.init(ctx, read_one, NoOp{});
       Rec r;
       int kslot = 0;
-      uint32_t kph = 0;
+      uint32_t kwrap = 0;
       while (!aborted && st.next(ctx, r, read_one, NoOp{})) {
+        if (r.g != my_g) {  // the other group's tile: only the ring position advances
+          if (++kslot == NSK) {
+            kslot = 0;
+            ++kwrap;
+          }
+          continue;
+        }
         uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
         const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
         if (r.j == 0) wait(&gb[kQFull], r.qi & 1u, aborted);
-        wait(&bars[kKFull + kslot], kph, aborted);
+        wait(&bars[kKFull + (kwrap & 1u) * kUmmaMaxStages + kslot], (kwrap >> 1) & 1u, aborted);
         wait(&gb[kSEmpty + b], ph ^ 1u, aborted);
         ptx::tc_fence_after();
         const unsigned char* kt = kring + kslot * kUmmaTileBytes;
@@ -563,18 +590,19 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         if (r.j == r.nt - 1) ptx::umma_commit(&gb[kQEmpty]);
         if (++kslot == NSK) {
           kslot = 0;
-          kph ^= 1u;
+          ++kwrap;
         }
       }
       // nothing may be in flight when tensor memory is freed
-      ptx::umma_commit(&bars[kDrainQK]);
+      ptx::umma_commit(&bars[kDrainQK + my_g]);
       bool drain_aborted = false;
-      wait(&bars[kDrainQK], 0, drain_aborted);
+      wait(&bars[kDrainQK + my_g], 0, drain_aborted);
       if (aborted || drain_aborted) flags[0] = 1;
     }
     __syncwarp();
-  } else if (warp == 11) {
+  } else if (warp == 11 || warp == 13) {
     // ============================ P.V issue ============================
+    // warp 11: group 0's tiles, warp 13: group 1's
     // Lane 0 waits and issues; the whole warp zeroes, in a tile whose last
     // 16-token step is partly past the end of the sequence, the V rows past
     // the end (they may hold stale or uninitialised data and P is 0 there).
@@ -583,15 +611,23 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, NP, 1, 1);
     Stream st;
     st.init(ctx, read_item, NoOp{});
+    const int my_g = warp == 13 ? 1 : 0;
     Rec r;
     int vslot = 0;
-    uint32_t vph = 0;
+    uint32_t vwrap = 0;
     while (!aborted && st.next(ctx, r, read_item, NoOp{})) {
+      if (r.g != my_g) {  // the other group's tile: only the ring position advances
+        if (++vslot == NSV) {
+          vslot = 0;
+          ++vwrap;
+        }
+        continue;
+      }
       uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
       const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
       unsigned char* vt = vring + vslot * kUmmaTileBytes;
       if (lane == 0) {
-        wait(&bars[kVFull + vslot], vph, aborted);
+        wait(&bars[kVFull + (vwrap & 1u) * kUmmaMaxStages + vslot], (vwrap >> 1) & 1u, aborted);
         wait(&gb[kPFull + b], ph, aborted);
         wait(&gb[kOEmpty + b], ph ^ 1u, aborted);
       }
@@ -623,13 +659,13 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       __syncwarp();
       if (++vslot == NSV) {
         vslot = 0;
-        vph ^= 1u;
+        ++vwrap;
       }
     }
     if (lane == 0) {
-      ptx::umma_commit(&bars[kDrainPV]);
+      ptx::umma_commit(&bars[kDrainPV + my_g]);
       bool drain_aborted = false;
-      wait(&bars[kDrainPV], 0, drain_aborted);
+      wait(&bars[kDrainPV + my_g], 0, drain_aborted);
       if (aborted || drain_aborted) flags[0] = 1;
     }
     __syncwarp();

@@ -71,6 +71,7 @@ EDGE_LENS = [0, 1, 7, 8, 15, 16, 17, 31, 32, 33, 63, 64, 65, 255, 256, 257, 511,
     ("f32", 64, 1, 16), ("f32", 64, 4, 8), ("f32", 128, 2, 32), ("f32", 128, 8, 16),
     ("bf16", 64, 8, 16), ("bf16", 64, 1, 1), ("bf16", 128, 1, 16), ("bf16", 128, 2, 8),
     ("bf16", 128, 4, 16), ("bf16", 128, 8, 32), ("bf16", 256, 4, 16), ("bf16", 256, 8, 64),
+    ("bf16", 128, 16, 16), ("bf16", 128, 4, 256),
 ])
 @pytest.mark.parametrize("partition_tokens", [0, 64])
 def test_shape_sweep_edge_lengths(ops, dtype, D, G, bs, partition_tokens):
