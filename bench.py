@@ -269,6 +269,74 @@ def reduce_over_ranks(times, counts, world: int, device=None):
 
 
 # --------------------------------------------------------------------------
+# secondary kernels (reported under "extras"; not part of the step)
+# --------------------------------------------------------------------------
+def _event_time_us(fn, iters: int, stream) -> float:
+    import torch
+    for _ in range(3):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1000.0 / iters
+
+
+def measure_extras(ops, dev, seed: int = 1420) -> dict:
+    """Multi-layer append and copy-on-write copy of a decode step, one launch
+    for all layers, against one launch per layer (algorithmic bytes: read +
+    write of every moved K/V element)."""
+    import torch
+    Lyr, T, Hkv, D, bs, NB, pairs_n = 32, 256, 8, 128, 16, 512, 64
+    g = torch.Generator(device=dev).manual_seed(seed)
+    stream = torch.cuda.current_stream(dev)
+    kc = torch.zeros((Lyr, NB, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    key = torch.randn((Lyr, T, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    val = torch.randn((Lyr, T, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.randperm(NB * bs, generator=g, device=dev)[:T].to(torch.int64)
+    perm = torch.randperm(NB, generator=g, device=dev)
+    pairs = torch.stack([perm[:pairs_n], perm[pairs_n:2 * pairs_n]], dim=1).to(torch.int64).contiguous()
+    append_b = Lyr * T * Hkv * D * 2 * 2 * 2
+    copy_b = Lyr * pairs_n * 2 * Hkv * bs * D * 2 * 2
+    t_app = _event_time_us(lambda: ops.pa_reshape_and_cache_layers(key, val, slots, kc, vc), 50, stream)
+    t_app1 = _event_time_us(lambda: [ops.pa_reshape_and_cache(key[i], val[i], slots, kc[i], vc[i])
+                                     for i in range(Lyr)], 20, stream)
+    t_cp = _event_time_us(lambda: ops.pa_copy_blocks_layers(kc, vc, pairs), 50, stream)
+    t_cp1 = _event_time_us(lambda: [ops.pa_copy_blocks(kc[i], vc[i], pairs) for i in range(Lyr)], 20, stream)
+    gbs = lambda b, us: round(b / (us * 1e-6) / 1e9, 1)
+    del kc, vc
+    # prefix caching (host): 64 requests of one 3000-token prefix + their own
+    # 32-token tails, keys hashed with SHA-256 in the allocator
+    rng = np.random.default_rng(seed)
+    prefix = rng.integers(0, 32000, size=3000)
+    reqs = [np.concatenate([prefix, rng.integers(0, 32000, size=32)]).astype(np.int32) for _ in range(64)]
+    pc = ops.BlockAllocator(8192, bs)
+    pc.enable_prefix_cache()
+    t0 = time.perf_counter()
+    hits = [pc.seq_create_prefix(r)[1] for r in reqs]
+    t_pc = (time.perf_counter() - t0) / len(reqs) * 1e6
+    used = pc.num_blocks - pc.num_free()
+    pc.close()
+    return {
+        "append_layers": {"layers": Lyr, "tokens": T, "bytes": append_b, "us": round(t_app, 2),
+                          "GB/s": gbs(append_b, t_app), "us_one_launch_per_layer": round(t_app1, 2)},
+        "copy_blocks_layers": {"layers": Lyr, "pairs": pairs_n, "bytes": copy_b, "us": round(t_cp, 2),
+                               "GB/s": gbs(copy_b, t_cp), "us_one_launch_per_layer": round(t_cp1, 2)},
+        "note": "bf16, 8 kv heads, head_dim 128, block 16; bytes = read + write of the moved K/V; "
+                "inputs smaller than L2 (the append's 67 MB, the copy's 268 MB straddles it)",
+        "prefix_cache": {"requests": len(reqs), "tokens_per_request": 3032,
+                         "cached_tokens_per_hit": int(hits[1]), "hits": int(sum(h > 0 for h in hits)),
+                         "blocks_used": int(used), "blocks_without_cache": 64 * 190,
+                         "us_per_request": round(t_pc, 1),
+                         "note": "host allocator, SHA-256 block keys; K/V prefill skipped for the "
+                                 "cached tokens"},
+    }
+
+
+# --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
 def gpu_arm(args):
@@ -483,6 +551,7 @@ def gpu_arm(args):
     e2e_val = sum_e2e_b / (t_e2e * 1e-3) / 1e9
     pt, ctas = ops.pa_decode_plan(B, H, Hkv, D, bs, "bf16", e2e_max_len, args.partition_tokens)
     clocks = sampler.summary()
+    extras = measure_extras(ops, dev) if world == 1 else None
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -523,6 +592,7 @@ def gpu_arm(args):
         "gpu_launches": 2 * K,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "extras": extras,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

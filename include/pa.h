@@ -104,6 +104,42 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache,
                          void* stream);
 
 /* ------------------------------------------------------------------------
+ * Multi-layer KV append and block copy -- [PA] "KV Cache 为什么难管理": a
+ * token's cache costs M_token = 2 * L * H_kv * d elements, K and V of every
+ * one of the model's L layers, so a step appends a token in every layer and
+ * a copy-on-write copies the block in every layer ([PA] "支持块级共享").
+ *
+ * One pool holds all layers: layer l of the K cache starts at
+ * k_cache + l * cache_layer_stride elements (likewise V), and layer l of the
+ * step's key/value input at key + l * kv_layer_stride elements.  Per layer
+ * the operation and layouts are those of pa_reshape_and_cache /
+ * pa_copy_blocks, applied to layers 0 .. num_layers-1 in one launch.
+ *   kv_layer_stride     elements between layers of key/value, >=
+ *                       num_tokens*num_kv_heads*head_dim
+ *   cache_layer_stride  elements between cache layers, >=
+ *                       num_blocks*num_kv_heads*block_size*head_dim
+ * Both strides times the element size must be multiples of 16 bytes (the
+ * strides are ignored when num_layers == 1).  1 <= num_layers <= 32767,
+ * else PA_ERR_INVALID_ARG.  The single-layer calls above are these calls
+ * with num_layers == 1.
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache_layers(const void* key, const void* value,
+                                      int64_t kv_layer_stride, int32_t num_layers,
+                                      int32_t num_tokens, const int64_t* slot_mapping,
+                                      void* k_cache, void* v_cache,
+                                      int64_t cache_layer_stride,
+                                      int32_t num_blocks, int32_t block_size,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      pa_dtype dtype, void* stream);
+
+pa_status pa_copy_blocks_layers(void* k_cache, void* v_cache,
+                                int64_t cache_layer_stride, int32_t num_layers,
+                                int32_t num_blocks, int32_t block_size,
+                                int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                const int64_t* block_pairs, int32_t num_pairs,
+                                void* stream);
+
+/* ------------------------------------------------------------------------
  * Paged decode attention -- [PA] "Block Table 如何工作": the kernel reads the
  * block table to turn logical block numbers into physical block ids, so each
  * sequence sees its K/V in token order; [PA] "不改变模型精度": the result is
@@ -246,7 +282,8 @@ pa_status pa_alloc_append_slots(pa_allocator* a, const int32_t* seqs, int32_t n,
  * fill); slots[0..n) receive the slots.  PA_ERR_INVALID_ARG if a copy would
  * be needed.  On PA_ERR_OOM nothing changes. */
 pa_status pa_alloc_append_tokens(pa_allocator* a, int32_t seq, int32_t n, int64_t* slots);
-/* Release every block of `seq` in table order; the id becomes invalid. */
+/* Release every block of `seq` in table order (last block first when
+ * prefix caching is on); the id becomes invalid. */
 pa_status pa_alloc_free_seq(pa_allocator* a, int32_t seq);
 /* Length of `seq` (-1 if it is not live). */
 int32_t   pa_alloc_seq_len(const pa_allocator* a, int32_t seq);
@@ -265,6 +302,53 @@ pa_status pa_alloc_export_tables(const pa_allocator* a, const int32_t* seqs, int
 pa_status pa_alloc_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
 /* Copy the live sequence ids, ascending, into out[0..cap); *n = count. */
 pa_status pa_alloc_live_seqs(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
+
+/* ------------------------------------------------------------------------
+ * Automatic prefix caching -- [KV02] section 4 "프리픽스 캐시": requests that
+ * share a leading part of their prompt share its K/V blocks, so that part
+ * needs no prefill.
+ *  - A full block's key is SHA-256(previous block's key, or 32 zero bytes for
+ *    the first block || the block's block_size token ids as little-endian
+ *    int32 || the request's extra bytes).  The extra bytes are the caller's
+ *    composition of what else separates requests (cache salt, adapter, input
+ *    hashes).  A key therefore stands for the whole prefix up to its block.
+ *  - Only full blocks are keyed; a key maps to the first block that held it.
+ *  - A block whose count drops to zero keeps its key and contents on the
+ *    free list.  Allocation takes the front of the list and drops that
+ *    block's key: least recently freed cached blocks go first, and a
+ *    released sequence queues its last block first, so tails are evicted
+ *    before the prefixes they extend.
+ *  - A cache hit takes its block off the free list.
+ * The decode, append and copy calls are unchanged: a hit is a block shared
+ * through the tables, like a fork.
+ * ---------------------------------------------------------------------- */
+/* Turn prefix caching on; only while no sequence exists and every block is
+ * free (PA_ERR_INVALID_ARG otherwise).  No effect if already on. */
+pa_status pa_alloc_enable_prefix_cache(pa_allocator* a);
+/* New tracked sequence holding token_ids[0..num_tokens).  Its leading full
+ * blocks are taken from the cache while their keys hit (up to the first
+ * miss).  The rest get fresh blocks, and every full block is keyed.
+ * slots[t] receives every token's slot; *cached_tokens receives the number
+ * of leading tokens whose K/V are already in the cache (a multiple of
+ * block_size), so the caller writes K/V only for tokens >= *cached_tokens.
+ * extra: extra_bytes bytes (may be NULL when 0).  On PA_ERR_OOM nothing
+ * changes; PA_ERR_INVALID_ARG if prefix caching is off. */
+pa_status pa_alloc_seq_create_prefix(pa_allocator* a, const int32_t* token_ids,
+                                     int32_t num_tokens, const void* extra, int32_t extra_bytes,
+                                     int32_t* seq, int32_t* cached_tokens, int64_t* slots);
+/* pa_alloc_append_tokens with the tokens' ids: a tracked sequence keys the
+ * blocks they complete.  (Appends without ids, pa_alloc_append_slot(s) and
+ * pa_alloc_append_tokens, end the keying of that sequence.) */
+pa_status pa_alloc_append_token_ids(pa_allocator* a, int32_t seq, const int32_t* token_ids,
+                                    int32_t n, int64_t* slots);
+/* Number of keyed blocks (in use or on the free list); -1 for NULL. */
+int32_t   pa_alloc_num_cached(const pa_allocator* a);
+/* Key of `block` -> key[32]; PA_ERR_INVALID_ARG if it holds none. */
+pa_status pa_alloc_block_key(const pa_allocator* a, int32_t block, uint8_t key[32]);
+
+/* SHA-256 (FIPS 180-4) of data[0..num_bytes) -> digest[32]; the block-key
+ * hash above, exported for checking. */
+pa_status pa_sha256(const void* data, size_t num_bytes, uint8_t digest[32]);
 
 #ifdef __cplusplus
 }

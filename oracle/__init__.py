@@ -15,19 +15,23 @@ Sources (the three pages on PagedAttention; cited by title and section):
            "不改变模型精度", "自检问题".
   [KV02]   "LLM KV cache 02 - serving engine KV" (ttlab.hopto.org), section 2
            "PagedAttention: KV 를 블록으로 나누기" (blocks, block table, sharing,
-           copy-on-write).
+           copy-on-write) and section 4 "프리픽스 캐시" (prefix caching).
 
 Modules:
   attention   paged decode attention (table walk + softmax(q K^T scale) V)
   cache_ops   slot write of new K/V, copy-on-write block copy
   allocator   block pool with a free list, reference counts, fork and COW
+  prefix_cache  automatic prefix caching on the pool (chained SHA-256 block
+              keys over full blocks, LRU eviction of freed cached blocks)
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values
 the pages print, closed forms and brute force; none is "parity unpinned".
 """
 from .attention import paged_decode, contiguous_attention, decode_bruteforce, gather_sequence
-from .cache_ops import reshape_and_cache, copy_blocks, slot_of
+from .cache_ops import (reshape_and_cache, copy_blocks, slot_of, reshape_and_cache_layers,
+                        copy_blocks_layers)
 from .allocator import OracleAllocator, AllocatorOOM, blocks_for, slack_for
+from .prefix_cache import OraclePrefixCacheAllocator, block_key
 
 __all__ = [
     "paged_decode", "contiguous_attention", "decode_bruteforce", "gather_sequence",

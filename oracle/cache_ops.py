@@ -57,3 +57,28 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
     for j, d in enumerate(dst):
         k_cache[d] = k_src[j]
         v_cache[d] = v_src[j]
+
+
+# Every layer of a model ([PA] "KV Cache 为什么难管理": a token costs
+# M_token = 2 * L * H_kv * d cache elements, K and V in each of the L layers):
+# a step appends its tokens in every layer, and a copy-on-write copies the
+# block in every layer.  The pool holds the layers as ``[L, NB, Hkv, bs, D]``
+# and the step's keys/values as ``[L, T, Hkv, D]``; each layer is written
+# exactly as the single-layer operation writes it, with the same slots or
+# pairs for every layer.
+
+def reshape_and_cache_layers(key, value, k_cache: np.ndarray, v_cache: np.ndarray,
+                             slot_mapping) -> None:
+    """Layer l of key/value into layer l of the caches, for every l, in place."""
+    if k_cache.ndim != 5 or key.ndim != 4 or key.shape[0] != k_cache.shape[0]:
+        raise ValueError("expected caches [L, NB, Hkv, bs, D] and key/value [L, T, Hkv, D]")
+    for layer in range(k_cache.shape[0]):
+        reshape_and_cache(key[layer], value[layer], k_cache[layer], v_cache[layer], slot_mapping)
+
+
+def copy_blocks_layers(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
+    """Every (src, dst) pair copied in every layer (pre-call state), in place."""
+    if k_cache.ndim != 5:
+        raise ValueError("expected caches [L, NB, Hkv, bs, D]")
+    for layer in range(k_cache.shape[0]):
+        copy_blocks(k_cache[layer], v_cache[layer], pairs)

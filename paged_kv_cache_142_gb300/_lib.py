@@ -35,6 +35,9 @@ SIGNATURES = {
     "pa_version": (C.c_char_p, []),
     "pa_reshape_and_cache": (i32, [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_copy_blocks": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, i32, vp]),
+    "pa_reshape_and_cache_layers": (i32, [vp, vp, i64, i32, i32, vp, vp, vp, i64, i32, i32, i32,
+                                          i32, i32, vp]),
+    "pa_copy_blocks_layers": (i32, [vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, i32, vp]),
     "pa_decode_workspace_size": (C.c_size_t, [i32, i32, i32, i32, i32, i32, i32, i32]),
     "pa_decode": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32,
                         C.c_float, i32, vp, C.c_size_t, vp]),
@@ -64,6 +67,12 @@ SIGNATURES = {
     "pa_alloc_export_tables": (i32, [vp, P_i32, i32, P_i32, i32, P_i32, i32]),
     "pa_alloc_free_list": (i32, [vp, P_i32, i32, P_i32]),
     "pa_alloc_live_seqs": (i32, [vp, P_i32, i32, P_i32]),
+    "pa_alloc_enable_prefix_cache": (i32, [vp]),
+    "pa_alloc_seq_create_prefix": (i32, [vp, P_i32, i32, vp, i32, P_i32, P_i32, P_i64]),
+    "pa_alloc_append_token_ids": (i32, [vp, i32, P_i32, i32, P_i64]),
+    "pa_alloc_num_cached": (i32, [vp]),
+    "pa_alloc_block_key": (i32, [vp, i32, C.c_char_p]),
+    "pa_sha256": (i32, [vp, C.c_size_t, C.c_char_p]),
 }
 
 _lib = None

@@ -28,6 +28,7 @@ using pa::DecodeParams;
 
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kDefaultPartTokens = 256;
+constexpr int32_t kMaxLayers = 32767;  // grid y of the copy kernel holds 2 * layers
 constexpr int64_t kSmCountHint = 152;  // GB300 SMs; only shapes the default partition size
 
 int dtype_bytes(pa_dtype d) {
@@ -288,38 +289,69 @@ const char* pa_status_string(pa_status s) {
 
 const char* pa_version(void) { return "pa_gb300 1.0 sm_103a"; }
 
-pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
-                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
-                               int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                               int32_t head_dim, pa_dtype dtype, void* stream) {
+pa_status pa_reshape_and_cache_layers(const void* key, const void* value, int64_t kv_layer_stride,
+                                      int32_t num_layers, int32_t num_tokens,
+                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                      int64_t cache_layer_stride, int32_t num_blocks,
+                                      int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                      pa_dtype dtype, void* stream) {
   pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
-  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_layers < 1 || num_layers > kMaxLayers) return PA_ERR_INVALID_ARG;
+  const int64_t e = dtype_bytes(dtype);
+  const int64_t kv_layer = static_cast<int64_t>(num_tokens) * num_kv_heads * head_dim;
+  const int64_t cache_layer = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size * head_dim;
+  if (num_layers > 1 && (kv_layer_stride < kv_layer || cache_layer_stride < cache_layer ||
+                         (kv_layer_stride * e) % 16 != 0 || (cache_layer_stride * e) % 16 != 0))
+    return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
   if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
     return PA_ERR_INVALID_ARG;
-  const int32_t row = head_dim * dtype_bytes(dtype);
-  cudaError_t e = pa::launch_reshape_and_cache(key, value, num_tokens, slot_mapping, k_cache,
-                                               v_cache, num_blocks, block_size, num_kv_heads, row,
-                                               static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const int32_t row = head_dim * static_cast<int32_t>(e);
+  cudaError_t err = pa::launch_reshape_and_cache(
+      key, value, num_layers > 1 ? kv_layer_stride * e : 0, num_layers, num_tokens, slot_mapping,
+      k_cache, v_cache, num_layers > 1 ? cache_layer_stride * e : 0, num_blocks, block_size,
+      num_kv_heads, row, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, pa_dtype dtype, void* stream) {
+  return pa_reshape_and_cache_layers(key, value, 0, 1, num_tokens, slot_mapping, k_cache, v_cache,
+                                     0, num_blocks, block_size, num_kv_heads, head_dim, dtype,
+                                     stream);
+}
+
+pa_status pa_copy_blocks_layers(void* k_cache, void* v_cache, int64_t cache_layer_stride,
+                                int32_t num_layers, int32_t num_blocks, int32_t block_size,
+                                int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                const int64_t* block_pairs, int32_t num_pairs, void* stream) {
+  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0 || num_layers < 1 || num_layers > kMaxLayers) return PA_ERR_INVALID_ARG;
+  const int64_t e = dtype_bytes(dtype);
+  const int64_t cache_layer = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size * head_dim;
+  if (num_layers > 1 && (cache_layer_stride < cache_layer || (cache_layer_stride * e) % 16 != 0))
+    return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  const int64_t block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * e;
+  cudaError_t err = pa::launch_copy_blocks(k_cache, v_cache,
+                                           num_layers > 1 ? cache_layer_stride * e : 0, num_layers,
+                                           num_blocks, block_bytes, block_pairs, num_pairs,
+                                           static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
                          int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
                          const int64_t* block_pairs, int32_t num_pairs, void* stream) {
-  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
-  if (st != PA_OK) return st;
-  if (num_pairs < 0) return PA_ERR_INVALID_ARG;
-  if (num_pairs == 0) return PA_OK;
-  if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
-  const int64_t block_bytes =
-      static_cast<int64_t>(num_kv_heads) * block_size * head_dim * dtype_bytes(dtype);
-  cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, num_blocks, block_bytes, block_pairs,
-                                         num_pairs, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa_copy_blocks_layers(k_cache, v_cache, 0, 1, num_blocks, block_size, num_kv_heads,
+                               head_dim, dtype, block_pairs, num_pairs, stream);
 }
 
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

@@ -12,26 +12,64 @@
 //
 // Policy where the pages leave it open: the free list starts in the caller's
 // order; allocation pops the front; a block whose count reaches zero is
-// pushed to the back; a sequence is released in table order.
+// pushed to the back; a sequence is released in table order (last block
+// first when prefix caching is on).
+#include <array>
 #include <cstdint>
-#include <deque>
+#include <cstring>
+#include <list>
 #include <map>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "pa.h"
+#include "sha256.h"
 
 namespace pa {
 
+// Automatic prefix caching ("llm-kv-cache-02-serving-engine-kv", section 4
+// "프리픽스 캐시"), enabled per allocator:
+//  * every full block of a tracked sequence gets a key, SHA-256 of the
+//    previous block's key (32 zero bytes for the first block), the block's
+//    token ids (little-endian int32) and the request's extra bytes (cache
+//    salt, adapter, ... as the caller composes them); a key therefore stands
+//    for the whole prefix up to and including its block;
+//  * only full blocks are keyed; a key maps to the first block that held it;
+//  * a new sequence reuses, block by block from the start, every block whose
+//    key is cached, up to the first miss (those tokens need no prefill);
+//  * a block whose count drops to zero keeps its key and content on the free
+//    queue; allocation takes the queue's front and evicts that block's key,
+//    so the least recently freed cached block goes first; a finished
+//    sequence's blocks are queued last block first, so tails are evicted
+//    before the prefixes they extend; a hit takes its block off the queue.
 class BlockAllocator {
  public:
+  using Key = std::array<uint8_t, 32>;
+  struct KeyHash {
+    size_t operator()(const Key& k) const {
+      size_t h;
+      std::memcpy(&h, k.data(), sizeof(h));
+      return h;
+    }
+  };
   struct Seq {
     std::vector<int32_t> table;
     int32_t len = 0;
+    // prefix caching: token ids and keys of the full blocks so far
+    bool track = false;
+    std::vector<int32_t> tokens;
+    std::vector<uint8_t> extra;
+    int32_t keyed = 0;  // leading full blocks whose key is known
+    Key last_key{};
   };
 
   BlockAllocator(int32_t num_blocks, int32_t block_size)
-      : num_blocks_(num_blocks), block_size_(block_size), ref_(num_blocks, 0) {}
+      : num_blocks_(num_blocks),
+        block_size_(block_size),
+        ref_(num_blocks, 0),
+        where_(num_blocks),
+        in_free_(num_blocks, 0) {}
 
   bool init_free_list(const int32_t* order) {
     std::vector<char> seen(num_blocks_, 0);
@@ -39,7 +77,7 @@ class BlockAllocator {
       int32_t b = order ? order[i] : i;
       if (b < 0 || b >= num_blocks_ || seen[b]) return false;
       seen[b] = 1;
-      free_.push_back(b);
+      push_free(b);
     }
     return true;
   }
@@ -54,6 +92,11 @@ class BlockAllocator {
     if (free_.empty()) return -1;
     int32_t b = free_.front();
     free_.pop_front();
+    in_free_[b] = 0;
+    if (pc_ && keyed_[b]) {  // the least recently freed cached block gives up its key
+      cached_.erase(key_[b]);
+      keyed_[b] = 0;
+    }
     ref_[b] = 1;
     return b;
   }
@@ -66,7 +109,7 @@ class BlockAllocator {
 
   pa_status decref(int32_t b) {
     if (!valid_block(b) || ref_[b] <= 0) return PA_ERR_INVALID_ARG;
-    if (--ref_[b] == 0) free_.push_back(b);
+    if (--ref_[b] == 0) push_free(b);
     return PA_OK;
   }
 
@@ -96,10 +139,156 @@ class BlockAllocator {
     return PA_OK;
   }
 
-  // Reserve the next token's slot (see pa_alloc_append_slot).
+  // Reserve the next token's slot (see pa_alloc_append_slot).  A tracked
+  // sequence appended to without its token id stops being keyed.
   pa_status append_slot(int32_t s, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
     Seq* q = find(s);
     if (!q) return PA_ERR_INVALID_ARG;
+    pa_status st = reserve(q, slot, cow_src, cow_dst);
+    if (st == PA_OK && q->track) {
+      q->track = false;
+      q->tokens.clear();
+    }
+    return st;
+  }
+
+  pa_status append_tokens(int32_t s, int32_t n, int64_t* slots, const int32_t* ids = nullptr) {
+    Seq* q = find(s);
+    if (!q || n < 0) return PA_ERR_INVALID_ARG;
+    // all-or-nothing: check the blocks needed and the sharing state first
+    const int32_t pos = q->len;
+    if (n == 0) return PA_OK;
+    if (pos % block_size_ != 0 && ref_[q->table[pos / block_size_]] > 1) return PA_ERR_INVALID_ARG;
+    const int64_t have = static_cast<int64_t>(q->table.size());
+    const int64_t need = (static_cast<int64_t>(pos) + n + block_size_ - 1) / block_size_;
+    if (need - have > static_cast<int64_t>(free_.size())) return PA_ERR_OOM;
+    for (int32_t j = 0; j < n; ++j) {
+      int32_t a, b;
+      pa_status st = reserve(q, &slots[j], &a, &b);
+      if (st != PA_OK) return st;  // unreachable after the checks above
+    }
+    if (q->track) {
+      if (ids) {
+        q->tokens.insert(q->tokens.end(), ids, ids + n);
+        register_full_blocks(q);
+      } else {
+        q->track = false;
+        q->tokens.clear();
+      }
+    }
+    return PA_OK;
+  }
+
+  pa_status free_seq(int32_t s) {
+    auto it = seqs_.find(s);
+    if (it == seqs_.end()) return PA_ERR_INVALID_ARG;
+    const std::vector<int32_t>& t = it->second.table;
+    if (pc_) {
+      for (auto b = t.rbegin(); b != t.rend(); ++b)  // tail first: evicted first
+        if (--ref_[*b] == 0) push_free(*b);
+    } else {
+      for (int32_t b : t)
+        if (--ref_[b] == 0) push_free(b);
+    }
+    seqs_.erase(it);
+    return PA_OK;
+  }
+
+  // ---- prefix caching ----
+  pa_status enable_prefix_cache() {
+    if (pc_) return PA_OK;
+    if (!seqs_.empty() || static_cast<int32_t>(free_.size()) != num_blocks_) return PA_ERR_INVALID_ARG;
+    pc_ = true;
+    key_.assign(num_blocks_, Key{});
+    keyed_.assign(num_blocks_, 0);
+    return PA_OK;
+  }
+  bool prefix_cache() const { return pc_; }
+  int32_t num_cached() const { return static_cast<int32_t>(cached_.size()); }
+  const Key* block_key(int32_t b) const { return valid_block(b) && pc_ && keyed_[b] ? &key_[b] : nullptr; }
+
+  Key key_of(const Key* prev, const int32_t* ids, const std::vector<uint8_t>& extra) {
+    // previous key || token ids (little-endian int32) || extra, hashed in one pass
+    std::vector<uint8_t>& buf = key_buf_;
+    buf.resize(32 + 4 * static_cast<size_t>(block_size_) + extra.size());
+    if (prev) std::memcpy(buf.data(), prev->data(), 32);
+    else std::memset(buf.data(), 0, 32);
+    uint8_t* p = buf.data() + 32;
+    for (int32_t j = 0; j < block_size_; ++j, p += 4) {
+      const uint32_t v = static_cast<uint32_t>(ids[j]);
+      p[0] = static_cast<uint8_t>(v);
+      p[1] = static_cast<uint8_t>(v >> 8);
+      p[2] = static_cast<uint8_t>(v >> 16);
+      p[3] = static_cast<uint8_t>(v >> 24);
+    }
+    if (!extra.empty()) std::memcpy(p, extra.data(), extra.size());
+    Sha256 h;
+    h.update(buf.data(), buf.size());
+    Key k;
+    h.finish(k.data());
+    return k;
+  }
+
+  pa_status seq_create_prefix(const int32_t* ids, int32_t n, const uint8_t* extra, int32_t extra_n,
+                              int32_t* seq, int32_t* cached_tokens, int64_t* slots) {
+    if (!pc_ || n < 0 || extra_n < 0 || (n > 0 && (!ids || !slots)) || (extra_n > 0 && !extra))
+      return PA_ERR_INVALID_ARG;
+    std::vector<uint8_t> ex(extra, extra + extra_n);
+    // longest run of cached leading full blocks (lookups only)
+    std::vector<int32_t> hits;
+    std::vector<Key> keys;
+    int32_t in_queue = 0;
+    for (int32_t j = 0; (static_cast<int64_t>(j) + 1) * block_size_ <= n; ++j) {
+      Key k = key_of(j ? &keys.back() : nullptr, ids + static_cast<int64_t>(j) * block_size_, ex);
+      auto it = cached_.find(k);
+      if (it == cached_.end()) break;
+      hits.push_back(it->second);
+      keys.push_back(k);
+      if (ref_[it->second] == 0) ++in_queue;
+    }
+    const int64_t need = (static_cast<int64_t>(n) + block_size_ - 1) / block_size_ - hits.size();
+    if (need > static_cast<int64_t>(free_.size()) - in_queue) return PA_ERR_OOM;
+    const int32_t s = seq_create();
+    Seq* q = find(s);
+    q->track = true;
+    q->extra = std::move(ex);
+    for (int32_t b : hits) {
+      if (ref_[b] == 0) take_free(b);
+      ++ref_[b];
+      q->table.push_back(b);
+    }
+    q->len = static_cast<int32_t>(hits.size()) * block_size_;
+    q->keyed = static_cast<int32_t>(hits.size());
+    if (!keys.empty()) q->last_key = keys.back();
+    q->tokens.assign(ids, ids + n);
+    for (int32_t t = q->len; t < n; ++t) {
+      int32_t a, b;
+      int64_t sl;
+      reserve(q, &sl, &a, &b);  // fresh blocks only: cannot fail after the check above
+    }
+    for (int32_t t = 0; t < n; ++t)
+      slots[t] = static_cast<int64_t>(q->table[t / block_size_]) * block_size_ + t % block_size_;
+    register_full_blocks(q);
+    *seq = s;
+    if (cached_tokens) *cached_tokens = static_cast<int32_t>(hits.size()) * block_size_;
+    return PA_OK;
+  }
+
+  const std::list<int32_t>& free_list() const { return free_; }
+  const std::map<int32_t, Seq>& seqs() const { return seqs_; }
+
+ private:
+  void push_free(int32_t b) {
+    free_.push_back(b);
+    where_[b] = std::prev(free_.end());
+    in_free_[b] = 1;
+  }
+  void take_free(int32_t b) {
+    free_.erase(where_[b]);
+    in_free_[b] = 0;
+  }
+
+  pa_status reserve(Seq* q, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
     const int32_t pos = q->len;
     const int32_t li = pos / block_size_;
     int32_t src = -1, dst = -1;
@@ -125,44 +314,40 @@ class BlockAllocator {
     return PA_OK;
   }
 
-  pa_status append_tokens(int32_t s, int32_t n, int64_t* slots) {
-    Seq* q = find(s);
-    if (!q || n < 0) return PA_ERR_INVALID_ARG;
-    // all-or-nothing: check the blocks needed and the sharing state first
-    const int32_t pos = q->len;
-    if (n == 0) return PA_OK;
-    if (pos % block_size_ != 0 && ref_[q->table[pos / block_size_]] > 1) return PA_ERR_INVALID_ARG;
-    const int64_t have = static_cast<int64_t>(q->table.size());
-    const int64_t need = (static_cast<int64_t>(pos) + n + block_size_ - 1) / block_size_;
-    if (need - have > static_cast<int64_t>(free_.size())) return PA_ERR_OOM;
-    for (int32_t j = 0; j < n; ++j) {
-      int32_t a, b;
-      pa_status st = append_slot(s, &slots[j], &a, &b);
-      if (st != PA_OK) return st;  // unreachable after the checks above
+  // Key every newly full block of a tracked sequence; a key already cached
+  // for another block leaves this block unkeyed (the first holder keeps it).
+  void register_full_blocks(Seq* q) {
+    if (!pc_ || !q->track) return;
+    const int32_t full = q->len / block_size_;
+    while (q->keyed < full) {
+      const int32_t j = q->keyed;
+      const Key k = key_of(j ? &q->last_key : nullptr,
+                           q->tokens.data() + static_cast<int64_t>(j) * block_size_, q->extra);
+      const int32_t b = q->table[j];
+      if (!keyed_[b] && cached_.find(k) == cached_.end()) {
+        key_[b] = k;
+        keyed_[b] = 1;
+        cached_.emplace(k, b);
+      }
+      q->last_key = k;
+      ++q->keyed;
     }
-    return PA_OK;
   }
 
-  pa_status free_seq(int32_t s) {
-    auto it = seqs_.find(s);
-    if (it == seqs_.end()) return PA_ERR_INVALID_ARG;
-    for (int32_t b : it->second.table) {
-      if (--ref_[b] == 0) free_.push_back(b);
-    }
-    seqs_.erase(it);
-    return PA_OK;
-  }
-
-  const std::deque<int32_t>& free_list() const { return free_; }
-  const std::map<int32_t, Seq>& seqs() const { return seqs_; }
-
- private:
   int32_t num_blocks_;
   int32_t block_size_;
   std::vector<int32_t> ref_;
-  std::deque<int32_t> free_;
+  std::list<int32_t> free_;
+  std::vector<std::list<int32_t>::iterator> where_;
+  std::vector<char> in_free_;
   std::map<int32_t, Seq> seqs_;
   int32_t next_seq_ = 0;
+  // prefix cache
+  bool pc_ = false;
+  std::vector<Key> key_;
+  std::vector<char> keyed_;
+  std::unordered_map<Key, int32_t, KeyHash> cached_;
+  std::vector<uint8_t> key_buf_;
 };
 
 }  // namespace pa
@@ -313,6 +498,34 @@ pa_status pa_alloc_free_list(const pa_allocator* a, int32_t* out, int32_t cap, i
   if (*n > cap || (*n > 0 && !out)) return PA_ERR_INVALID_ARG;
   int32_t k = 0;
   for (int32_t b : fl) out[k++] = b;
+  return PA_OK;
+}
+
+pa_status pa_alloc_enable_prefix_cache(pa_allocator* a) {
+  return a ? a->impl.enable_prefix_cache() : PA_ERR_INVALID_ARG;
+}
+
+pa_status pa_alloc_seq_create_prefix(pa_allocator* a, const int32_t* token_ids, int32_t num_tokens,
+                                     const void* extra, int32_t extra_bytes, int32_t* seq,
+                                     int32_t* cached_tokens, int64_t* slots) {
+  if (!a || !seq) return PA_ERR_INVALID_ARG;
+  return a->impl.seq_create_prefix(token_ids, num_tokens, static_cast<const uint8_t*>(extra),
+                                   extra_bytes, seq, cached_tokens, slots);
+}
+
+pa_status pa_alloc_append_token_ids(pa_allocator* a, int32_t seq, const int32_t* token_ids,
+                                    int32_t n, int64_t* slots) {
+  if (!a || n < 0 || (n > 0 && (!slots || !token_ids))) return PA_ERR_INVALID_ARG;
+  return a->impl.append_tokens(seq, n, slots, token_ids);
+}
+
+int32_t pa_alloc_num_cached(const pa_allocator* a) { return a ? a->impl.num_cached() : -1; }
+
+pa_status pa_alloc_block_key(const pa_allocator* a, int32_t block, uint8_t key[32]) {
+  if (!a || !key) return PA_ERR_INVALID_ARG;
+  const pa::BlockAllocator::Key* k = a->impl.block_key(block);
+  if (!k) return PA_ERR_INVALID_ARG;
+  std::memcpy(key, k->data(), 32);
   return PA_OK;
 }
 

@@ -6,6 +6,12 @@
 // Block copy ("PagedAttention", section "支持块级共享"): a shared block is
 // copied to a fresh one before a branch writes different content into it.
 //
+// Both also run over the L layers of a pool that holds every layer's cache
+// at a fixed stride, in one launch: a step's append writes a token's K/V in
+// every layer ("PagedAttention", section "KV Cache 为什么难管理": a token
+// costs 2 * L * H_kv * d elements of cache), and a copy-on-write copies the
+// block in every layer.
+//
 // Both are pure data movement in 16-byte vectors: consecutive threads move
 // consecutive 16-byte chunks of a token row (slot write) or of a whole block
 // (copy), so every global access is coalesced.  Out-of-range slots / blocks
@@ -15,14 +21,22 @@
 namespace pa {
 namespace {
 
+// Layer l of every buffer starts l * stride 16-byte chunks after layer 0
+// (one pool holding all layers); blockIdx.y is the layer.
 __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
-                             int32_t num_tokens, const int64_t* __restrict__ slots,
-                             uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                             int64_t kv_layer_chunks, int32_t num_tokens,
+                             const int64_t* __restrict__ slots, uint4* __restrict__ k_cache,
+                             uint4* __restrict__ v_cache, int64_t cache_layer_chunks,
                              int64_t num_slots, int32_t bs, int32_t hkv, int32_t chunks) {
   const int32_t per_token = hkv * chunks;  // 16-byte chunks of one token's K (all kv heads)
   const int64_t total = static_cast<int64_t>(num_tokens) * per_token;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t layer = blockIdx.y;
+  key += layer * kv_layer_chunks;
+  value += layer * kv_layer_chunks;
+  k_cache += layer * cache_layer_chunks;
+  v_cache += layer * cache_layer_chunks;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += stride) {
     const int64_t t = i / per_token;
@@ -39,14 +53,15 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// blockIdx.x: pair; blockIdx.y: layer * 2 + (0 K, 1 V); blockIdx.z: slice of the block
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                       int32_t num_blocks, int64_t chunks_per_block,
+                       int64_t cache_layer_chunks, int32_t num_blocks, int64_t chunks_per_block,
                        const int64_t* __restrict__ pairs) {
   const int64_t src = pairs[2 * static_cast<int64_t>(blockIdx.x)];
   const int64_t dst = pairs[2 * static_cast<int64_t>(blockIdx.x) + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return;
-  uint4* base = blockIdx.y ? v_cache : k_cache;
+  uint4* base = ((blockIdx.y & 1u) ? v_cache : k_cache) + (blockIdx.y >> 1) * cache_layer_chunks;
   const uint4* s = base + src * chunks_per_block;
   uint4* d = base + dst * chunks_per_block;
   const int64_t step = static_cast<int64_t>(blockDim.x) * gridDim.z;
@@ -57,35 +72,43 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kv_layer_bytes,
+                                     int32_t num_layers, int32_t num_tokens,
                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
-                                     int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                                     int32_t row_bytes, cudaStream_t stream) {
+                                     int64_t cache_layer_bytes, int32_t num_blocks,
+                                     int32_t block_size, int32_t num_kv_heads, int32_t row_bytes,
+                                     cudaStream_t stream) {
   const int32_t chunks = row_bytes / 16;
   const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * chunks;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
-  const int64_t cap = 152 * 16;  // grid-stride beyond ~16 CTAs per SM
+  // about 16 CTAs per SM in all, grid-striding beyond that
+  int64_t cap = 152 * 16 / num_layers;
+  if (cap < 1) cap = 1;
   if (blocks > cap) blocks = cap;
-  reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), num_tokens, slot_mapping,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      static_cast<int64_t>(num_blocks) * block_size, block_size, num_kv_heads, chunks);
+  reshape_and_cache_kernel<<<dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(num_layers)),
+                             threads, 0, stream>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), kv_layer_bytes / 16,
+      num_tokens, slot_mapping, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      cache_layer_bytes / 16, static_cast<int64_t>(num_blocks) * block_size, block_size,
+      num_kv_heads, chunks);
   return cudaGetLastError();
 }
 
-cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks,
-                               int64_t block_bytes, const int64_t* pairs, int32_t num_pairs,
-                               cudaStream_t stream) {
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t cache_layer_bytes,
+                               int32_t num_layers, int32_t num_blocks, int64_t block_bytes,
+                               const int64_t* pairs, int32_t num_pairs, cudaStream_t stream) {
   const int64_t chunks = block_bytes / 16;
   const int threads = 256;
   // about 8 chunks (128 bytes) per thread per CTA
   int64_t split = (chunks + threads * 8 - 1) / (threads * 8);
   if (split < 1) split = 1;
   if (split > 64) split = 64;
-  dim3 grid(static_cast<unsigned>(num_pairs), 2, static_cast<unsigned>(split));
+  dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(2 * num_layers),
+            static_cast<unsigned>(split));
   copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4*>(k_cache),
-                                                   static_cast<uint4*>(v_cache), num_blocks, chunks,
+                                                   static_cast<uint4*>(v_cache),
+                                                   cache_layer_bytes / 16, num_blocks, chunks,
                                                    pairs);
   return cudaGetLastError();
 }

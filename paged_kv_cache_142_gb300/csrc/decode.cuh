@@ -70,13 +70,17 @@ bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInf
 // Tensor-core kernel (bf16, head_dim 128) for a GQA group, or nullptr.
 const void* decode_umma_fn(int group);
 
-cudaError_t launch_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
+// Cache ops over num_layers layers of one pool (layer strides in bytes,
+// multiples of 16); one layer is num_layers == 1.
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kv_layer_bytes,
+                                     int32_t num_layers, int32_t num_tokens,
                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
-                                     int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                                     int32_t row_bytes, cudaStream_t stream);
+                                     int64_t cache_layer_bytes, int32_t num_blocks,
+                                     int32_t block_size, int32_t num_kv_heads, int32_t row_bytes,
+                                     cudaStream_t stream);
 
-cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks,
-                               int64_t block_bytes, const int64_t* pairs, int32_t num_pairs,
-                               cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t cache_layer_bytes,
+                               int32_t num_layers, int32_t num_blocks, int64_t block_bytes,
+                               const int64_t* pairs, int32_t num_pairs, cudaStream_t stream);
 
 }  // namespace pa

@@ -79,6 +79,46 @@ def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
             "pa_copy_blocks")
 
 
+def _layer_cache_dims(k_cache, v_cache):
+    _need(k_cache.dim() == 5 and v_cache.shape == k_cache.shape, "caches must be [L, NB, Hkv, bs, D]")
+    _need(k_cache.dtype == v_cache.dtype and k_cache.is_cuda and v_cache.is_cuda,
+          "caches must be CUDA tensors of one dtype")
+    _need(k_cache[0].is_contiguous() and v_cache[0].is_contiguous()
+          and k_cache.stride(0) == v_cache.stride(0), "each cache layer must be contiguous, "
+          "with the same layer stride for K and V")
+    return tuple(k_cache.shape)
+
+
+def pa_reshape_and_cache_layers(key, value, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Every layer at once: key/value ``[L, T, Hkv, D]`` into the caches
+    ``[L, NB, Hkv, bs, D]`` at ``slot_mapping[T]`` (the same slots in every layer)."""
+    Lyr, NB, Hkv, bs, D = _layer_cache_dims(k_cache, v_cache)
+    T = key.shape[1]
+    _need(key.shape == (Lyr, T, Hkv, D) and value.shape == key.shape, "key/value must be [L, T, Hkv, D]")
+    _need(key.dtype == k_cache.dtype and value.dtype == k_cache.dtype, "key/value dtype != cache dtype")
+    _need(key[0].is_contiguous() and value[0].is_contiguous() and key.stride(0) == value.stride(0),
+          "each key/value layer must be contiguous, with the same layer stride")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T and slot_mapping.is_cuda,
+          "slot_mapping must be a CUDA int64 tensor of num_tokens entries")
+    L.check(_LIB.pa_reshape_and_cache_layers(
+        key.data_ptr(), value.data_ptr(), key.stride(0), Lyr, T, slot_mapping.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), k_cache.stride(0), NB, bs, Hkv, D,
+        dtype_code(k_cache.dtype), _stream(stream)), "pa_reshape_and_cache_layers")
+
+
+def pa_copy_blocks_layers(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """cache[l, dst] = cache[l, src] for every layer l and row (src, dst) of ``block_pairs``."""
+    Lyr, NB, Hkv, bs, D = _layer_cache_dims(k_cache, v_cache)
+    n = block_pairs.shape[0] if block_pairs.numel() else 0
+    if n:
+        _need(block_pairs.dtype == torch.int64 and block_pairs.is_cuda and block_pairs.is_contiguous()
+              and block_pairs.shape == (n, 2), "block_pairs must be a contiguous CUDA int64 [n, 2]")
+    L.check(_LIB.pa_copy_blocks_layers(k_cache.data_ptr(), v_cache.data_ptr(), k_cache.stride(0), Lyr,
+                                       NB, bs, Hkv, D, dtype_code(k_cache.dtype),
+                                       block_pairs.data_ptr() if n else None, n, _stream(stream)),
+            "pa_copy_blocks_layers")
+
+
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                              max_context_len, partition_tokens=0) -> int:
     n = _LIB.pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -317,3 +357,46 @@ class BlockAllocator:
         refs = [self.refcount(b) for b in range(self.num_blocks)]
         seqs = {s: (self.block_table(s), self.seq_len(s)) for s in self.live_seqs()}
         return self.free_list(), refs, seqs
+
+    # ---- prefix caching (pa_alloc_enable_prefix_cache and friends) ----
+    def enable_prefix_cache(self) -> None:
+        L.check(_LIB.pa_alloc_enable_prefix_cache(self._h), "pa_alloc_enable_prefix_cache")
+
+    def seq_create_prefix(self, token_ids, extra: bytes = b""):
+        """(seq, cached_tokens, slots[n]) for a new tracked sequence of these tokens."""
+        ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+        n = len(ids)
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        s, cached = C.c_int32(-1), C.c_int32(0)
+        ex = C.create_string_buffer(bytes(extra), max(len(extra), 1))
+        _acheck(_LIB.pa_alloc_seq_create_prefix(self._h, _p32(ids) if n else None, n,
+                                                C.cast(ex, C.c_void_p) if extra else None, len(extra),
+                                                C.byref(s), C.byref(cached), _p64(slots)),
+                "pa_alloc_seq_create_prefix")
+        return s.value, cached.value, slots[:n]
+
+    def append_token_ids(self, seq: int, token_ids) -> np.ndarray:
+        ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+        n = len(ids)
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        _acheck(_LIB.pa_alloc_append_token_ids(self._h, seq, _p32(ids) if n else None, n, _p64(slots)),
+                "pa_alloc_append_token_ids")
+        return slots[:n]
+
+    def num_cached(self) -> int:
+        return _LIB.pa_alloc_num_cached(self._h)
+
+    def block_key(self, block: int):
+        """The block's 32-byte key, or None if it holds none."""
+        buf = C.create_string_buffer(32)
+        if _LIB.pa_alloc_block_key(self._h, block, buf) != L.PA_OK:
+            return None
+        return buf.raw
+
+
+def sha256(data: bytes) -> bytes:
+    """pa_sha256 (FIPS 180-4) of ``data``."""
+    buf = C.create_string_buffer(32)
+    src = C.create_string_buffer(bytes(data), max(len(data), 1))
+    L.check(_LIB.pa_sha256(C.cast(src, C.c_void_p), len(data), buf), "pa_sha256")
+    return buf.raw

@@ -76,3 +76,65 @@ def test_copy_blocks_skips_out_of_range_and_empty(ops):
     k0[4] = k0[3]
     v0[4] = v0[3]
     assert torch.equal(kc, k0) and torch.equal(vc, v0)
+
+
+@pytest.mark.parametrize("dtype,Lyr,bs,Hkv,D", [("bf16", 4, 16, 8, 128), ("bf16", 3, 8, 2, 64),
+                                                ("f32", 2, 16, 4, 64), ("bf16", 1, 16, 8, 128)])
+def test_layered_append_and_copy_bit_exact(ops, dtype, Lyr, bs, Hkv, D):
+    """All layers in one launch, against the oracle applied layer by layer;
+    the caches live in one pool with a padded layer stride."""
+    NB, T = 24, 13
+    rng = np.random.default_rng(100 + Lyr * bs + D)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    cache0 = W.Values.from_f32(rng.standard_normal((Lyr, NB, Hkv, bs, D)).astype(np.float32), dtype)
+    key = W.Values.from_f32(rng.standard_normal((Lyr, T, Hkv, D)).astype(np.float32), dtype)
+    val = W.Values.from_f32(rng.standard_normal((Lyr, T, Hkv, D)).astype(np.float32), dtype)
+    # pool with one spare block of padding per layer: layer stride > one layer's elements
+    pool_k = torch.zeros((Lyr, NB + 1, Hkv, bs, D), dtype=dt, device="cuda")
+    pool_v = torch.zeros_like(pool_k)
+    kc, vc = pool_k[:, :NB], pool_v[:, :NB]
+    kc.copy_(to_device(cache0))
+    vc.copy_(-to_device(cache0))
+    perm = rng.permutation(NB * bs)
+    slots = np.concatenate([perm[:T - 2], [-1, NB * bs + 5]]).astype(np.int64)
+    ops.pa_reshape_and_cache_layers(to_device(key), to_device(val), torch.from_numpy(slots).cuda(), kc, vc)
+    bperm = rng.permutation(NB)
+    pairs = np.stack([bperm[:5], bperm[5:10]], axis=1).astype(np.int64)
+    ops.pa_copy_blocks_layers(kc, vc, torch.from_numpy(pairs).cuda())
+    ek = raw_bits(cache0.bits).copy()
+    ev = raw_bits(cache_bits(-to_device(cache0)))
+    keep = (slots >= 0) & (slots < NB * bs)
+    oracle.reshape_and_cache_layers(raw_bits(key.bits)[:, keep], raw_bits(val.bits)[:, keep], ek, ev,
+                                    slots[keep])
+    oracle.copy_blocks_layers(ek, ev, pairs)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache_bits(kc.contiguous()), ek)
+    assert np.array_equal(cache_bits(vc.contiguous()), ev)
+    assert not pool_k[:, NB].any() and not pool_v[:, NB].any()  # padding untouched
+
+
+def test_layered_calls_equal_per_layer_calls(ops):
+    Lyr, NB, Hkv, bs, D, T = 5, 16, 8, 16, 128, 32
+    g = torch.Generator(device="cuda").manual_seed(5)
+    key = torch.randn((Lyr, T, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+    val = torch.randn((Lyr, T, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+    slots = torch.randperm(NB * bs, device="cuda", generator=g)[:T].to(torch.int64)
+    a_k = torch.zeros((Lyr, NB, Hkv, bs, D), dtype=torch.bfloat16, device="cuda")
+    a_v = torch.zeros_like(a_k)
+    b_k, b_v = a_k.clone(), a_v.clone()
+    ops.pa_reshape_and_cache_layers(key, val, slots, a_k, a_v)
+    for layer in range(Lyr):
+        ops.pa_reshape_and_cache(key[layer], val[layer], slots, b_k[layer], b_v[layer])
+    torch.cuda.synchronize()
+    assert torch.equal(a_k, b_k) and torch.equal(a_v, b_v)
+
+
+def test_layered_argument_errors(ops):
+    from paged_kv_cache_142_gb300 import _lib as L
+    lib = L.load()
+    # layer stride shorter than a layer, or not a multiple of 16 bytes
+    assert lib.pa_reshape_and_cache_layers(1, 1, 10, 2, 4, 1, 16, 16, 16 * 2 * 16 * 64, 16, 16, 2, 64, 1,
+                                           None) == L.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks_layers(16, 16, 16 * 2 * 16 * 64 + 1, 2, 16, 16, 2, 64, 1, 16, 1,
+                                     None) == L.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks_layers(16, 16, 0, 0, 16, 16, 2, 64, 1, 16, 1, None) == L.PA_ERR_INVALID_ARG

@@ -325,6 +325,41 @@ def test_copy_blocks_uses_pre_call_state():
         oracle.copy_blocks(kc, vc, [(1, 2), (3, 2)])  # repeated destination
 
 
+def test_layered_append_writes_m_token_elements_per_token():
+    """[PA] "KV Cache 为什么难管理": one token's cache is M_token = 2*L*H_kv*d
+    elements; every layer receives its own K/V at the same slot."""
+    Lyr, NB, Hkv, bs, D = 3, 5, 2, 4, 3
+    kc = np.zeros((Lyr, NB, Hkv, bs, D))
+    vc = np.zeros_like(kc)
+    T = 3
+    # key[l, t] = 100*(l+1) + (t+1), value = its negative
+    key = (100 * np.arange(1, Lyr + 1)[:, None, None, None] + np.arange(1, T + 1)[None, :, None, None]
+           ) * np.ones((Lyr, T, Hkv, D))
+    val = -key
+    slots = [2 * bs + 1, -1, 4 * bs + 3]
+    oracle.reshape_and_cache_layers(key, val, kc, vc, slots)
+    written = 2  # token 1 is padding
+    assert np.count_nonzero(kc) + np.count_nonzero(vc) == written * 2 * Lyr * Hkv * D
+    for layer in range(Lyr):
+        assert (kc[layer, 2, :, 1] == 100 * (layer + 1) + 1).all()
+        assert (vc[layer, 4, :, 3] == -(100 * (layer + 1) + 3)).all()
+    with pytest.raises(ValueError):
+        oracle.reshape_and_cache_layers(key[:2], val[:2], kc, vc, slots)  # layer count mismatch
+
+
+def test_layered_copy_copies_each_layer_from_its_own_source():
+    rng = np.random.default_rng(11)
+    kc = rng.standard_normal((4, 6, 2, 4, 3))
+    vc = rng.standard_normal((4, 6, 2, 4, 3))
+    k0, v0 = kc.copy(), vc.copy()
+    oracle.copy_blocks_layers(kc, vc, [(1, 4), (3, 0)])
+    for layer in range(4):
+        assert np.array_equal(kc[layer, 4], k0[layer, 1]) and np.array_equal(vc[layer, 0], v0[layer, 3])
+        for b in (1, 2, 3, 5):
+            assert np.array_equal(kc[layer, b], k0[layer, b]) and np.array_equal(vc[layer, b], v0[layer, b])
+    assert not np.array_equal(kc[0, 4], kc[1, 4])  # layers stay distinct
+
+
 # --------------------------------------------------------------------------
 # allocator: refcounts, fork, copy-on-write, shared-prefix scenario
 # --------------------------------------------------------------------------
