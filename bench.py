@@ -308,6 +308,27 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     t_cp1 = _event_time_us(lambda: [ops.pa_copy_blocks(kc[i], vc[i], pairs) for i in range(Lyr)], 20, stream)
     gbs = lambda b, us: round(b / (us * 1e-6) / 1e9, 1)
     del kc, vc
+    # paged prefill (tensor cores): 16 prompts of 2048 tokens, causal
+    S_, n_, Hq_ = 16, 2048, 32
+    nb_seq = n_ // bs
+    NBp = S_ * nb_seq
+    kpp = torch.randn((NBp, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    vpp = torch.randn((NBp, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    tab = torch.randperm(NBp, generator=g, device=dev).to(torch.int32).reshape(S_, nb_seq).contiguous()
+    qp = torch.randn((S_ * n_, Hq_, D), generator=g, device=dev).to(torch.bfloat16)
+    op = torch.empty_like(qp)
+    cu = torch.arange(0, (S_ + 1) * n_, n_, dtype=torch.int32, device=dev)
+    st0 = torch.zeros(S_, dtype=torch.int32, device=dev)
+    stat = torch.zeros(1, dtype=torch.int32, device=dev)
+    t_pf = _event_time_us(lambda: ops.pa_prefill(op, qp, kpp, vpp, cu, st0, tab, 1.0 / math.sqrt(D), Hkv, n_,
+                                                 status=stat), 10, stream)
+    flops = S_ * 2.0 * D * Hq_ * n_ * (n_ + 1)
+    pf_tflops = flops / (t_pf * 1e-6) / 1e12
+    pf_ok = int(stat.item()) == 0
+    del kpp, vpp, qp, op
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
     # prefix caching (host): 64 requests of one 3000-token prefix + their own
     # 32-token tails, keys hashed with SHA-256 in the allocator
     rng = np.random.default_rng(seed)
@@ -327,6 +348,11 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
                                "GB/s": gbs(copy_b, t_cp), "us_one_launch_per_layer": round(t_cp1, 2)},
         "note": "bf16, 8 kv heads, head_dim 128, block 16; bytes = read + write of the moved K/V; "
                 "inputs smaller than L2 (the append's 67 MB, the copy's 268 MB straddles it)",
+        "prefill": {"prompts": S_, "tokens_per_prompt": n_, "q_heads": Hq_, "kv_heads": Hkv, "head_dim": D,
+                    "us": round(t_pf, 1), "TFLOP/s": round(pf_tflops, 1),
+                    "frac_of_bf16_peak": round(pf_tflops / bf16_peak, 4), "bf16_peak_tflops": bf16_peak,
+                    "status_ok": pf_ok,
+                    "flops": "causal algorithmic: 2*D*H*n*(n+1) per prompt (Q.K^T and P.V)"},
         "prefix_cache": {"requests": len(reqs), "tokens_per_request": 3032,
                          "cached_tokens_per_hit": int(hits[1]), "hits": int(sum(h > 0 for h in hits)),
                          "blocks_used": int(used), "blocks_without_cache": 64 * 190,

@@ -231,6 +231,42 @@ pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, void* strea
 pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_status);
 
 /* ------------------------------------------------------------------------
+ * Paged prefill attention -- [PA] "KV Cache 为什么难管理": the prefill phase
+ * processes a prompt's tokens together; [PA] "Block Table 如何工作": every
+ * token reads its sequence's K/V through the block table.  Chunked prefill
+ * (a prompt split over several calls) is the same call with a later start.
+ *
+ * Sequence i's chunk is q[cu_q[i] .. cu_q[i+1]) (tokens); its token j sits
+ * at position p = q_start[i] + j of the sequence and attends causally:
+ *   K_t = k_cache[block_tables[i*max_blocks_per_seq + t/block_size]][g][t%block_size]
+ *   out[cu_q[i]+j][h][:] = sum_{t <= p} softmax_t(scale * q[cu_q[i]+j][h]·K_t) * V_t
+ * with g = h / (num_q_heads / num_kv_heads).  The chunk's own K/V must be in
+ * the cache already (pa_reshape_and_cache first).  Accumulation is fp32.
+ *
+ *   out          device, [num_tokens][num_q_heads][128] of out_dtype
+ *   q            device, [num_tokens][num_q_heads][128] bf16
+ *   cu_q         device, int32 [num_seqs + 1], non-decreasing, cu_q[0] >= 0,
+ *                cu_q[num_seqs] <= num_tokens
+ *   q_start      device, int32 [num_seqs]
+ *   max_q_len    host, >= every chunk length (sizes the launch)
+ *   status       device int32, caller-zeroed, or NULL: receives
+ *                PA_ERR_INVALID_ARG for a chunk outside q or beyond the table,
+ *                or for a table entry outside the pool (never read: block 0
+ *                is read instead), and PA_ERR_DEVICE_TIMEOUT if a bounded wait
+ *                expired.
+ * Supported: bf16 K/V and q, head_dim 128, block_size 8..256 (power of two),
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}; PA_ERR_UNSUPPORTED
+ * otherwise.  num_tokens, num_seqs or max_q_len == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, int32_t num_tokens,
+                     const int32_t* cu_q, const int32_t* q_start, int32_t num_seqs,
+                     int32_t max_q_len, int32_t num_q_heads,
+                     const void* k_cache, const void* v_cache, int32_t num_blocks,
+                     int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                     pa_dtype dtype, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     float scale, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Host block allocator -- [vLLM2] block-table section and [KV02] section 2:
  * fixed-size blocks handed out on demand from anywhere in the pool; [PA]
  * "Block Table 如何工作": full blocks trigger a new allocation, freed blocks

@@ -27,7 +27,8 @@ Modules:
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values
 the pages print, closed forms and brute force; none is "parity unpinned".
 """
-from .attention import paged_decode, contiguous_attention, decode_bruteforce, gather_sequence
+from .attention import (paged_decode, contiguous_attention, decode_bruteforce, gather_sequence,
+                        paged_prefill)
 from .cache_ops import (reshape_and_cache, copy_blocks, slot_of, reshape_and_cache_layers,
                         copy_blocks_layers)
 from .allocator import OracleAllocator, AllocatorOOM, blocks_for, slack_for

@@ -129,3 +129,31 @@ def decode_bruteforce(q, k_cache, v_cache, block_tables, context_lens, scale: fl
             rows.append(o)
         res.append(rows)
     return res
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, cu_q, q_start, scale: float,
+                  num_kv_heads: int) -> np.ndarray:
+    """Prefill attention through the block tables, causal.
+
+    [PA] "KV Cache 为什么难管理": the prefill phase runs the prompt's tokens
+    together; each token's query attends to the keys of its own position and
+    every earlier one.  Sequence i's chunk is q[cu_q[i]:cu_q[i+1]] and its
+    token j sits at position q_start[i] + j (a later start is the next piece
+    of a chunked prefill).  Returns float64 [T, H, D]; rows outside every
+    chunk stay zero.
+    """
+    q = np.asarray(q)
+    T, H, D = q.shape
+    G = H // num_kv_heads
+    out = np.zeros((T, H, D), dtype=np.float64)
+    for i in range(len(cu_q) - 1):
+        b, e = int(cu_q[i]), int(cu_q[i + 1])
+        start = int(q_start[i])
+        last = start + (e - b)
+        K = gather_sequence(k_cache, block_tables[i], last)
+        V = gather_sequence(v_cache, block_tables[i], last)
+        for j in range(e - b):
+            p = start + j
+            out[b + j] = contiguous_attention(q[b + j], K[:p + 1], V[:p + 1], scale)
+    assert G * num_kv_heads == H
+    return out

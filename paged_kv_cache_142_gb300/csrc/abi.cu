@@ -354,6 +354,82 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32
                                head_dim, dtype, block_pairs, num_pairs, stream);
 }
 
+// 2-D map over the queries [num_tokens, num_q_heads * 128] (bf16): boxes of
+// 64 elements (one 128-byte swizzle span) by box_rows tokens.
+bool encode_q_tokens(CUtensorMap* m, const void* base, uint64_t tokens, uint64_t row_elems,
+                     uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {row_elems, tokens};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, int32_t num_tokens,
+                     const int32_t* cu_q, const int32_t* q_start, int32_t num_seqs,
+                     int32_t max_q_len, int32_t num_q_heads, const void* k_cache,
+                     const void* v_cache, int32_t num_blocks, int32_t block_size,
+                     int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq, float scale,
+                     int32_t* status, void* stream) {
+  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0 || num_seqs < 0 || max_q_len < 0 || num_q_heads <= 0 ||
+      max_blocks_per_seq <= 0 || !(scale > 0.f) || dtype_bytes(out_dtype) == 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if (dtype != PA_DTYPE_BF16 || head_dim != 128 || block_size < 8 || !pa::prefill_umma_fn(G))
+    return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0 || num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (!out || !q || !cu_q || !q_start || !k_cache || !v_cache || !block_tables)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int64_t cache_rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
+  if (cache_rows >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+  const int TQ = 128 / G;
+  pa::PrefillParams p{};
+  p.out = out;
+  p.out_bf16 = out_dtype == PA_DTYPE_BF16 ? 1 : 0;
+  p.cu_q = cu_q;
+  p.q_start = q_start;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.num_tokens = num_tokens;
+  p.tiles_per_seq = (max_q_len + TQ - 1) / TQ;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  const int64_t items = static_cast<int64_t>(num_seqs) * num_kv_heads * p.tiles_per_seq;
+  if (items >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+  const void* fn = pa::prefill_umma_fn(G);
+  const int smem = pa::prefill_umma_smem_bytes();
+  int ctas = 0;
+  st = prepare_kernel(fn, 256, smem, &ctas);
+  if (st != PA_OK) return st;
+  if (ctas > items) ctas = static_cast<int>(items);
+  CUtensorMap tmq, tmk, tmv;
+  const uint32_t box_rows = static_cast<uint32_t>(block_size < 128 ? block_size : 128);
+  if (!encode_q_tokens(&tmq, q, static_cast<uint64_t>(num_tokens),
+                       static_cast<uint64_t>(num_q_heads) * 128, static_cast<uint32_t>(TQ)) ||
+      !encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
+      !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows))
+    return PA_ERR_CUDA;
+  void* args[] = {&p, &tmq, &tmk, &tmv};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(256), args,
+                                   static_cast<size_t>(smem), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t block_size, pa_dtype dtype,
                                 int32_t max_context_len, int32_t partition_tokens) {

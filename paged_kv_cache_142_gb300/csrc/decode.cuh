@@ -70,6 +70,27 @@ bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInf
 // Tensor-core kernel (bf16, head_dim 128) for a GQA group, or nullptr.
 const void* decode_umma_fn(int group);
 
+// Paged prefill (tensor cores, bf16, head_dim 128, block size >= 8).
+struct PrefillParams {
+  void* out;
+  int32_t out_bf16;
+  const int32_t* cu_q;     // [num_seqs + 1] chunk offsets into q / out (tokens)
+  const int32_t* q_start;  // [num_seqs] position of each chunk's first token
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_tokens;
+  int32_t tiles_per_seq;   // ceil(max chunk length / tokens per tile)
+  float scale_log2;
+  int32_t* status;         // device error word (may be null)
+};
+const void* prefill_umma_fn(int group);
+int prefill_umma_smem_bytes();
+
 // Cache ops over num_layers layers of one pool (layer strides in bytes,
 // multiples of 16); one layer is num_layers == 1.
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kv_layer_bytes,

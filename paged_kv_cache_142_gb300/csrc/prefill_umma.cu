@@ -1,0 +1,466 @@
+// Paged prefill attention on the 5th-generation tensor cores (sm_103a):
+// bf16 K/V and queries, head_dim 128, block size >= 8, GQA group G in
+// {1, 2, 4, 8, 16}.
+//
+// The other phase of a step ("PagedAttention", section "KV Cache
+// 为什么难管理": prefill processes the prompt's tokens together, decode one
+// token at a time).  A chunk of a sequence's tokens -- its whole prompt, or
+// the next piece of a chunked prefill -- attends causally to its sequence's
+// history through the block table ("Block Table 如何工作"): the token at
+// position p sees keys 0 .. p, including the chunk's own, whose K/V are
+// appended before the call.
+//
+// Unlike decode, the contraction here is dense: a tile puts 128 query rows
+// (TQ = 128 / G tokens x the G query heads of one kv head) against 128 keys,
+//   S[128 rows x 128 keys]   = Q[128 x 128 dims] . K_tile^T
+//   O[128 rows x 128 dims]  += P[128 x 128 keys] . V_tile
+// each eight tcgen05.mma (M = N = 128, K = 16) with fp32 accumulators in
+// tensor memory (S double-buffered, then O).  P enters the second product as
+// bf16 hi = bf16(p) and lo = bf16(p - hi), two passes of eight MMAs, so each
+// probability keeps about 16 bits.
+//
+// One CTA per SM, 256 threads, persistent over (tile of TQ tokens, sequence,
+// kv head) items, later (longer) tiles first:
+//  * warp 0 loads the item's query rows (2-D TMA boxes, one per head and
+//    64-dim half) and its K tiles (one 4-D TMA box per block, as in decode)
+//    into a 2-stage ring; warp 2 loads the V tiles likewise;
+//  * warp 1 issues Q.K^T of tile t, then P.V of tile t - 1 (so the softmax
+//    of tile t overlaps the products), zeroing first the V rows past the end
+//    inside the last 16-key step of the item's last tile;
+//  * warps 4-7 own tensor-memory lanes 0-127, one query row per thread: per
+//    tile they read the row of S twice (max, then exponentials), mask keys
+//    past the row's position, run the online softmax in fp32 (log2 domain)
+//    and write P hi/lo to shared memory (128-byte swizzle, K-major).  The
+//    running max is the reference of P and O and is raised only when a row's
+//    max grows by more than 2^8 (then the warp rescales its O rows in tensor
+//    memory), so most tiles leave O alone.  At the item's end each thread
+//    divides its O row by the row sum and stores it.
+// Every mbarrier wait is bounded; on expiry the roles stop, the issuer
+// drains, tensor memory is freed and PA_ERR_DEVICE_TIMEOUT is written to the
+// caller's status word.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "decode.cuh"
+#include "ptx.cuh"
+
+namespace pa {
+
+namespace prefill_detail {
+
+constexpr int kThreads = 256;
+constexpr int kTileBytes = 32768;
+constexpr int kOffQ = 0;
+constexpr int kOffPhi = 32768;
+constexpr int kOffPlo = 65536;
+constexpr int kOffK = 98304;                 // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
+constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align the base
+constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only past 2^8
+
+// barriers
+constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
+              kSFull = 10, kSEmpty = 12, kPFull = 14, kPVDone = 15, kOEmpty = 16, kDrain = 17,
+              kNumBars = 18;
+
+struct Item {
+  int seq, kvh, qb, tok0, ntq, pos0, kend, ntiles;
+};
+
+__device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, Item& it) {
+  const int hkv = p.num_kv_heads;
+  const int per_tile = p.num_seqs * hkv;
+  const int tile = p.tiles_per_seq - 1 - w / per_tile;
+  const int rem = w - (w / per_tile) * per_tile;
+  it.seq = rem / hkv;
+  it.kvh = rem - it.seq * hkv;
+  const int TQ = 128 / G;
+  it.qb = p.cu_q[it.seq];
+  const int n = p.cu_q[it.seq + 1] - it.qb;
+  it.tok0 = tile * TQ;
+  if (n <= 0 || it.tok0 >= n) return false;  // no tokens in this tile
+  const int q0 = p.q_start[it.seq];
+  if (it.qb < 0 || it.qb + n > p.num_tokens || q0 < 0 ||
+      static_cast<int64_t>(q0) + n > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
+    if (p.status) atomicExch(p.status, kDevErrInvalidArg);  // offsets outside q or the table
+    return false;
+  }
+  it.ntq = min(TQ, n - it.tok0);
+  it.pos0 = q0 + it.tok0;
+  it.kend = it.pos0 + it.ntq;
+  it.ntiles = (it.kend + 127) / 128;
+  return true;
+}
+
+__device__ __forceinline__ void wait(uint64_t* bar, uint32_t parity, bool& aborted) {
+  if (!aborted && !ptx::mbar_wait(bar, parity, kWaitLimitNs)) aborted = true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+}  // namespace prefill_detail
+
+template <int G>
+__global__ void __launch_bounds__(prefill_detail::kThreads, 1)
+    paged_prefill_umma_kernel(const __grid_constant__ PrefillParams p,
+                              const __grid_constant__ CUtensorMap tm_q,
+                              const __grid_constant__ CUtensorMap tm_k,
+                              const __grid_constant__ CUtensorMap tm_v) {
+  using namespace prefill_detail;
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
+  constexpr int TQ = 128 / G;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* qbuf = smem + kOffQ;
+  unsigned char* phi = smem + kOffPhi;
+  unsigned char* plo = smem + kOffPlo;
+  unsigned char* kring = smem + kOffK;
+  unsigned char* vring = smem + kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] a role gave up
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hkv = p.num_kv_heads, bs = p.block_size;
+  const int bs_log = __ffs(bs) - 1;
+  const int items = p.num_seqs * hkv * p.tiles_per_seq;
+
+  if (tid == 0) {
+    ptx::mbar_init(&bars[kQFull], 1);
+    ptx::mbar_init(&bars[kQEmpty], 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bars[kKFull + s], 1);
+      ptx::mbar_init(&bars[kKEmpty + s], 1);
+      ptx::mbar_init(&bars[kVFull + s], 1);
+      ptx::mbar_init(&bars[kVEmpty + s], 1);
+      ptx::mbar_init(&bars[kSFull + s], 1);
+      ptx::mbar_init(&bars[kSEmpty + s], 4);
+    }
+    ptx::mbar_init(&bars[kPFull], 4);
+    ptx::mbar_init(&bars[kPVDone], 1);
+    ptx::mbar_init(&bars[kOEmpty], 4);
+    ptx::mbar_init(&bars[kDrain], 1);
+    flags[0] = 0;
+    ptx::mbar_init_fence();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 512);  // S[2] x 128 columns, then O x 128
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool aborted = false;
+
+  if (warp == 0 || warp == 2) {
+    // ============ loaders: warp 0 queries + K tiles, warp 2 V tiles ============
+    const bool is_v = warp == 2;
+    if (lane == 0) {
+      ptx::prefetch_tensormap(is_v ? &tm_v : &tm_k);
+      if (!is_v) ptx::prefetch_tensormap(&tm_q);
+    }
+    const uint64_t pol_kv = ptx::policy_evict_first();
+    const uint64_t pol_q = ptx::policy_evict_normal();
+    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+    unsigned char* ring = is_v ? vring : kring;
+    uint64_t* full = bars + (is_v ? kVFull : kKFull);
+    uint64_t* empty = bars + (is_v ? kVEmpty : kKEmpty);
+    const int box_rows = min(bs, 128);
+    uint32_t ic = 0, fc = 0;  // items, tile fills
+    for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
+      Item it;
+      if (!item_at(p, w, G, it)) continue;
+      if (!is_v && lane == 0) {
+        wait(&bars[kQEmpty], (ic & 1u) ^ 1u, aborted);
+        ptx::mbar_arrive_expect_tx(&bars[kQFull], 2u * 128u * 128u);
+        for (int g = 0; g < G; ++g)
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_2d(qbuf + h * 16384 + g * TQ * 128, &tm_q, (it.kvh * G + g) * 128 + h * 64,
+                             it.qb + it.tok0, &bars[kQFull], pol_q);
+      }
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
+      for (int t = 0; t < it.ntiles && !aborted; ++t, ++fc) {
+        const int slot = static_cast<int>(fc & 1u);
+        const uint32_t ph = (fc >> 1) & 1u;
+        const int nv = min(128, it.kend - t * 128);
+        const int nbox = (nv + box_rows - 1) / box_rows;
+        int row = 0;
+        if (lane < nbox) {
+          const int tok = t * 128 + lane * box_rows;
+          const int lb = tok >> bs_log;
+          int phys = trow[lb];
+          if (phys < 0 || phys >= p.num_blocks) {  // never read outside the pool
+            if (p.status) atomicExch(p.status, kDevErrInvalidArg);
+            phys = 0;
+          }
+          row = ((phys * hkv + it.kvh) << bs_log) + (tok - (lb << bs_log));
+        }
+        if (lane == 0) {
+          wait(&empty[slot], ph ^ 1u, aborted);
+          ptx::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * box_rows * 256));
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        if (!aborted && lane < nbox)
+          ptx::tma_load_4d(ring + slot * kTileBytes + lane * box_rows * 256, tm, 0, 0, 0, row >> 3,
+                           &full[slot], pol_kv);
+        __syncwarp();
+      }
+      ++ic;
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issue ============================
+    constexpr uint32_t kIdQK = ptx::idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, 128, 0, 1);
+    uint32_t ic = 0, kc = 0, vc = 0, sc = 0, tc = 0;
+    auto pv = [&](const Item& it, int t) {
+      const int vslot = static_cast<int>(vc & 1u);
+      unsigned char* vt = vring + vslot * kTileBytes;
+      if (lane == 0) {
+        wait(&bars[kVFull + vslot], (vc >> 1) & 1u, aborted);
+        wait(&bars[kPFull], tc & 1u, aborted);
+        if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
+      }
+      aborted = __shfl_sync(0xffffffffu, aborted, 0);
+      const int nv = min(128, it.kend - t * 128);
+      const int nks = (nv + 15) / 16;
+      if (!aborted && (nv & 15)) {  // V rows past the end inside the last 16-key step
+        const int nrows = nks * 16 - nv;
+        for (int c = lane; c < nrows * 16; c += 32) {
+          const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+          *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        ptx::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (!aborted && lane == 0) {
+        ptx::tc_fence_after();
+        const uint32_t od = tmem + 256;
+        for (int ks = 0; ks < nks; ++ks) {
+          const uint64_t bd = ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128);
+          const int a_off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          ptx::umma_bf16(od, ptx::smem_desc(phi + a_off, 16, 1024, ptx::kLayoutSw128), bd, kIdPV,
+                         t > 0 || ks > 0);
+          ptx::umma_bf16(od, ptx::smem_desc(plo + a_off, 16, 1024, ptx::kLayoutSw128), bd, kIdPV, 1);
+        }
+        ptx::umma_commit(&bars[kPVDone]);
+        ptx::umma_commit(&bars[kVEmpty + vslot]);
+      }
+      __syncwarp();
+      ++vc;
+      ++tc;
+    };
+    for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
+      Item it;
+      if (!item_at(p, w, G, it)) continue;
+      if (lane == 0) wait(&bars[kQFull], ic & 1u, aborted);
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int b = static_cast<int>(sc & 1u);
+        const int kslot = static_cast<int>(kc & 1u);
+        if (lane == 0) {
+          wait(&bars[kKFull + kslot], (kc >> 1) & 1u, aborted);
+          wait(&bars[kSEmpty + b], ((sc >> 1) & 1u) ^ 1u, aborted);
+          if (!aborted) {
+            ptx::tc_fence_after();
+            const unsigned char* kt = kring + kslot * kTileBytes;
+            const uint32_t sd = tmem + b * 128;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int h = kk >> 2, k4 = kk & 3;
+              ptx::umma_bf16(sd, ptx::smem_desc(qbuf + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
+                             ptx::smem_desc(kt + h * 1024 + k4 * 32, 16, 2048, ptx::kLayoutSw128), kIdQK,
+                             kk > 0);
+            }
+            ptx::umma_commit(&bars[kSFull + b]);
+            ptx::umma_commit(&bars[kKEmpty + kslot]);
+            if (t == it.ntiles - 1) ptx::umma_commit(&bars[kQEmpty]);
+          }
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        ++kc;
+        ++sc;
+        if (aborted) break;
+        if (t > 0) pv(it, t - 1);
+      }
+      if (!aborted) pv(it, it.ntiles - 1);
+      ++ic;
+    }
+    if (lane == 0) {  // nothing may be in flight when tensor memory is freed
+      ptx::umma_commit(&bars[kDrain]);
+      bool drain_aborted = false;
+      wait(&bars[kDrain], 0, drain_aborted);
+      if (aborted || drain_aborted) flags[0] = 1;
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============ softmax / epilogue: one query row per thread ============
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const int g = r / TQ, trow = r - (r / TQ) * TQ;
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, tc = 0;
+    // 16-byte chunk c (keys 8c .. 8c+7) of this row in a 128-byte-swizzled,
+    // K-major [2 halves][128 rows][128 B] tile
+    auto chunk_addr = [&](unsigned char* base, int c) -> unsigned char* {
+      return base + (c >> 3) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
+    };
+    for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
+      Item it;
+      if (!item_at(p, w, G, it)) continue;
+      const bool valid = trow < it.ntq;
+      const int limit = valid ? it.pos0 + trow + 1 : 0;  // keys visible to this row
+      float m_ref = -CUDART_INF_F, l = 0.f;
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int b = static_cast<int>(sc & 1u);
+        wait(&bars[kSFull + b], (sc >> 1) & 1u, aborted);
+        aborted = __any_sync(0xffffffffu, aborted);
+        if (aborted) break;
+        ptx::tc_fence_after();
+        const uint32_t sbase = tmem + lane_base + b * 128;
+        const int key0 = t * 128;
+        // pass 1: the row's max over this tile
+        float mt = -CUDART_INF_F;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          ptx::TmemLd<32>::run(sbase + c * 32, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (key0 + c * 32 + j < limit) mt = fmaxf(mt, __uint_as_float(v[j]) * sl2);
+        }
+        // P and O are free once the previous tile's P.V is done
+        if (t > 0) {
+          wait(&bars[kPVDone], (tc - 1) & 1u, aborted);
+          ptx::tc_fence_after();
+        }
+        const float mn = fmaxf(m_ref, mt);
+        bool rescale = t > 0 && mn > m_ref + kRescaleLog2;
+        float alpha = 1.f;
+        if (t == 0) {
+          m_ref = mn;
+        } else if (rescale) {
+          alpha = exp2f(m_ref - mn);
+          m_ref = mn;
+          l *= alpha;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {  // warp-collective O rescale in tensor memory
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            ptx::TmemLd<32>::run(tmem + lane_base + 256 + c * 32, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            ptx::tmem_st32(tmem + lane_base + 256 + c * 32, v);
+          }
+          ptx::tmem_wait_st();
+        }
+        // pass 2: p = 2^(s - m_ref) (0 for masked keys), row sum, P hi/lo rows
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          ptx::TmemLd<32>::run(sbase + c * 32, v);
+          ptx::tmem_wait_ld();
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float pr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const bool vis = key0 + c * 32 + j + e < limit;
+              pr[e] = vis ? exp2f(__uint_as_float(v[j + e]) * sl2 - m_ref) : 0.f;
+              l += pr[e];
+            }
+            const float h0 = __bfloat162float(__float2bfloat16_rn(pr[0]));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(pr[1]));
+            hi[j >> 1] = pack_bf16(h0, h1);
+            lo[j >> 1] = pack_bf16(pr[0] - h0, pr[1] - h1);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            *reinterpret_cast<uint4*>(chunk_addr(phi, c * 4 + q)) =
+                make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+            *reinterpret_cast<uint4*>(chunk_addr(plo, c * 4 + q)) =
+                make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&bars[kSEmpty + b]);
+          ptx::mbar_arrive(&bars[kPFull]);
+        }
+        ++sc;
+        ++tc;
+      }
+      if (aborted) break;
+      // epilogue: O row / row sum
+      wait(&bars[kPVDone], (tc - 1) & 1u, aborted);
+      aborted = __any_sync(0xffffffffu, aborted);
+      if (aborted) break;
+      ptx::tc_fence_after();
+      const float inv = valid && l > 0.f ? 1.f / l : 0.f;
+      const int64_t orow = (static_cast<int64_t>(it.qb + it.tok0 + trow) * p.num_q_heads + it.kvh * G + g) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::TmemLd<32>::run(tmem + lane_base + 256 + c * 32, v);
+        ptx::tmem_wait_ld();
+        if (valid) {
+          if (p.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+              dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                   __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
+    }
+  }
+
+  // ============================ teardown ============================
+  if (aborted) flags[0] = 1;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, 512);
+  if (tid == 0 && flags[0] && p.status) atomicExch(p.status, kDevErrTimeout);
+}
+
+const void* prefill_umma_fn(int group) {
+  switch (group) {
+    case 1: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<1>);
+    case 2: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<2>);
+    case 4: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<4>);
+    case 8: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<8>);
+    case 16: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<16>);
+    default: return nullptr;
+  }
+}
+
+int prefill_umma_smem_bytes() { return prefill_detail::kSmemBytes; }
+
+}  // namespace pa

@@ -119,6 +119,28 @@ def pa_copy_blocks_layers(k_cache, v_cache, block_pairs, stream=None) -> None:
             "pa_copy_blocks_layers")
 
 
+def pa_prefill(out, q, k_cache, v_cache, cu_q, q_start, block_tables, scale, num_kv_heads,
+               max_q_len, status=None, stream=None) -> None:
+    """Causal paged attention of each sequence's chunk ``q[cu_q[i]:cu_q[i+1]]``
+    (positions from ``q_start[i]``) over its K/V through ``block_tables``."""
+    NB, Hkv, bs, D = _cache_dims(k_cache, v_cache)
+    _need(Hkv == num_kv_heads, "num_kv_heads does not match the cache")
+    T, H, Dq = q.shape
+    _need(Dq == D and out.shape == q.shape, "q / out must be [T, H, D]")
+    _need(q.is_contiguous() and out.is_contiguous() and q.dtype == k_cache.dtype, "q must be contiguous, cache dtype")
+    S = cu_q.numel() - 1
+    _need(cu_q.dtype == torch.int32 and q_start.dtype == torch.int32 and q_start.numel() == S
+          and block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] >= S,
+          "cu_q [S+1], q_start [S], block_tables [S, M] must be int32")
+    _need(block_tables.is_contiguous(), "block_tables must be contiguous")
+    L.check(_LIB.pa_prefill(out.data_ptr(), dtype_code(out.dtype), q.data_ptr(), T, cu_q.data_ptr(),
+                            q_start.data_ptr(), S, int(max_q_len), H, k_cache.data_ptr(), v_cache.data_ptr(),
+                            NB, bs, Hkv, D, dtype_code(k_cache.dtype), block_tables.data_ptr(),
+                            block_tables.shape[1], float(scale),
+                            status.data_ptr() if status is not None else None, _stream(stream)),
+            "pa_prefill")
+
+
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                              max_context_len, partition_tokens=0) -> int:
     n = _LIB.pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

@@ -294,6 +294,80 @@ def test_shared_prefix_equals_private_copies():
 
 
 # --------------------------------------------------------------------------
+# prefill (causal): [PA] "KV Cache 为什么难管理" -- prefill runs the prompt's
+# tokens together, each attending to its own position and earlier ones
+# --------------------------------------------------------------------------
+def _prefill_case(rng, lens, starts, H=4, Hkv=2, D=8, bs=4, NB=40):
+    kc = rng.standard_normal((NB, Hkv, bs, D))
+    vc = rng.standard_normal((NB, Hkv, bs, D))
+    perm = rng.permutation(NB)
+    maxb = max(-(-(s + n) // bs) for s, n in zip(starts, lens))
+    tables = np.zeros((len(lens), maxb), dtype=np.int64)
+    k = 0
+    for i, (s, n) in enumerate(zip(starts, lens)):
+        nb = -(-(s + n) // bs)
+        tables[i, :nb] = perm[k:k + nb]
+        k += nb
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    q = rng.standard_normal((int(cu[-1]), H, D))
+    return q, kc, vc, tables, cu, np.asarray(starts), Hkv
+
+
+def test_prefill_first_token_returns_its_value():
+    rng = np.random.default_rng(31)
+    q, kc, vc, tables, cu, st, Hkv = _prefill_case(rng, [5], [0])
+    out = oracle.paged_prefill(q, kc, vc, tables, cu, st, 0.7, Hkv)
+    v0 = vc[tables[0, 0], :, 0, :]
+    G = q.shape[1] // Hkv
+    for h in range(q.shape[1]):
+        assert np.allclose(out[0, h], v0[h // G], atol=1e-15)
+
+
+def test_prefill_is_causal_and_last_row_is_decode():
+    rng = np.random.default_rng(32)
+    q, kc, vc, tables, cu, st, Hkv = _prefill_case(rng, [9], [0])
+    out = oracle.paged_prefill(q, kc, vc, tables, cu, st, 0.5, Hkv)
+    # later keys do not change earlier rows: overwrite positions 5.. and recompute
+    kc2, vc2 = kc.copy(), vc.copy()
+    bs = kc.shape[2]
+    for t in range(5, 9):
+        kc2[tables[0, t // bs], :, t % bs] += 3.0
+        vc2[tables[0, t // bs], :, t % bs] -= 2.0
+    out2 = oracle.paged_prefill(q, kc2, vc2, tables, cu, st, 0.5, Hkv)
+    assert np.array_equal(out[:5], out2[:5]) and not np.allclose(out[5:], out2[5:])
+    # the last token of the prompt is a decode step over the whole prompt
+    dec = oracle.paged_decode(q[8:9], kc, vc, tables, [9], 0.5, Hkv)
+    assert np.allclose(out[8], dec[0], atol=1e-13)
+
+
+def test_chunked_prefill_equals_whole_prompt():
+    """A prompt split into chunks (later starts) gives the rows of one call."""
+    rng = np.random.default_rng(33)
+    q, kc, vc, tables, cu, st, Hkv = _prefill_case(rng, [13], [0])
+    whole = oracle.paged_prefill(q, kc, vc, tables, cu, st, 0.6, Hkv)
+    parts = oracle.paged_prefill(q, kc, vc, np.repeat(tables, 3, axis=0), [0, 4, 9, 13], [0, 4, 9], 0.6, Hkv)
+    assert np.allclose(whole, parts, atol=1e-14)
+
+
+def test_prefill_bruteforce_on_tiny():
+    rng = np.random.default_rng(34)
+    q, kc, vc, tables, cu, st, Hkv = _prefill_case(rng, [3, 2], [0, 5], H=2, Hkv=1, D=3, bs=2, NB=12)
+    out = oracle.paged_prefill(q, kc, vc, tables, cu, st, 0.9, Hkv)
+    import math
+    for i in range(2):
+        for j in range(int(cu[i + 1] - cu[i])):
+            p = int(st[i]) + j
+            for h in range(2):
+                s = [0.9 * sum(q[cu[i] + j, h, d] * kc[tables[i, t // 2], 0, t % 2, d] for d in range(3))
+                     for t in range(p + 1)]
+                m = max(s)
+                w = [math.exp(x - m) for x in s]
+                for d in range(3):
+                    ref = sum(w[t] * vc[tables[i, t // 2], 0, t % 2, d] for t in range(p + 1)) / sum(w)
+                    assert abs(out[cu[i] + j, h, d] - ref) < 1e-12
+
+
+# --------------------------------------------------------------------------
 # slot write and block copy
 # --------------------------------------------------------------------------
 def test_reshape_and_cache_positions_and_skip():
