@@ -326,6 +326,42 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     pf_tflops = flops / (t_pf * 1e-6) / 1e12
     pf_ok = int(stat.item()) == 0
     del kpp, vpp, qp, op
+    # shared-prefix decode: the beam-search workload's last step, 64 sequences
+    # = one 3000-token prompt + 32 tokens of their own (the prompt's 187 full
+    # blocks shared by all), plain decode against one group of 64
+    Sb, pref, own = 64, 3000, 32
+    NBs = pref // bs + 1 + Sb * (own // bs + 2)
+    al = ops.BlockAllocator(NBs, bs)
+    root = al.seq_create()
+    al.append_tokens(root, pref)
+    beams = [al.fork(root) for _ in range(Sb)]
+    al.free_seq(root)
+    for _ in range(own):
+        al.append_slots(beams)
+    tb, ln = al.export_tables(beams, (pref + own) // bs + 2)
+    al.close()
+    ksp = torch.randn((NBs, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    vsp = torch.randn((NBs, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    qs = torch.randn((Sb, Hq_, D), generator=g, device=dev).to(torch.bfloat16)
+    osp = torch.empty((Sb, Hq_, D), dtype=torch.bfloat16, device=dev)
+    t_tb, t_ln = torch.from_numpy(tb).to(dev), torch.from_numpy(ln).to(dev)
+    mlen = int(ln.max())
+    wsd = ops.make_workspace(Sb, Hq_, Hkv, D, bs, "bf16", mlen, device=dev)
+    gs = torch.tensor([0, Sb], dtype=torch.int32, device=dev)
+    shared = (pref // bs) * bs
+    pl_ = torch.tensor([shared], dtype=torch.int32, device=dev)
+    st_sp = torch.zeros(1, dtype=torch.int32, device=dev)
+    wss = ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D), Hkv, mlen, gs, pl_, Sb,
+                                      shared, status=st_sp)
+    t_plain = _event_time_us(lambda: ops.pa_decode(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D), Hkv, mlen,
+                                                   wsd), 50, stream)
+    t_shared = _event_time_us(lambda: ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D),
+                                                                  Hkv, mlen, gs, pl_, Sb, shared, workspace=wss,
+                                                                  status=st_sp), 50, stream)
+    logical = int(ln.sum()) * Hkv * D * 2 * 2 + 2 * Sb * Hq_ * D * 2
+    unique_blocks = len(set(tb[:, :int(ln.max()) // bs + 1].ravel().tolist()))
+    sp_ok = int(st_sp.item()) == 0
+    del ksp, vsp
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
@@ -353,6 +389,12 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
                     "frac_of_bf16_peak": round(pf_tflops / bf16_peak, 4), "bf16_peak_tflops": bf16_peak,
                     "status_ok": pf_ok,
                     "flops": "causal algorithmic: 2*D*H*n*(n+1) per prompt (Q.K^T and P.V)"},
+        "shared_prefix_decode": {"sequences": Sb, "shared_tokens": shared, "own_tokens": pref + own - shared,
+                                 "logical_bytes": logical, "unique_kv_bytes": unique_blocks * Hkv * bs * D * 2 * 2,
+                                 "us_pa_decode": round(t_plain, 2), "us_shared_prefix": round(t_shared, 2),
+                                 "logical_GB/s_pa_decode": gbs(logical, t_plain),
+                                 "logical_GB/s_shared_prefix": gbs(logical, t_shared), "status_ok": sp_ok,
+                                 "note": "the unique K/V fits in L2: logical bytes are what the tables name"},
         "prefix_cache": {"requests": len(reqs), "tokens_per_request": 3032,
                          "cached_tokens_per_hit": int(hits[1]), "hits": int(sum(h > 0 for h in hits)),
                          "blocks_used": int(used), "blocks_without_cache": 64 * 190,

@@ -231,6 +231,53 @@ pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, void* strea
 pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_status);
 
 /* ------------------------------------------------------------------------
+ * Shared-prefix decode -- [PA] "支持块级共享", [KV02] section 2: sequences
+ * that share a prefix (a common prompt, parallel samples, beams) point at the
+ * same physical blocks; this decode reads each shared block once per group
+ * instead of once per sequence.  The result is that of pa_decode.
+ *
+ * The batch's sequences form groups of consecutive indices:
+ * group j is [group_start[j], group_start[j+1]).  The first prefix_len[j]
+ * tokens of every member are the same blocks: the first prefix_len[j] /
+ * block_size entries of every member's table are equal.  A sequence that
+ * shares nothing is a group of its own with prefix 0.  The call runs
+ *  (1) every group's queries (members x heads of a kv head, as the rows of
+ *      dense 128-row tiles) against its prefix, split into partitions;
+ *  (2) every member's own tokens [prefix_len, context_len);
+ *  (3) a log-sum-exp merge of the partial results into out.
+ *   q, out           device, [num_seqs][num_q_heads][128]; q bf16
+ *   group_start      device, int32 [num_groups + 1], group_start[0] == 0,
+ *                    non-decreasing, group_start[num_groups] == num_seqs
+ *   prefix_len       device, int32 [num_groups], multiples of block_size,
+ *                    <= every member's context length
+ *   max_group_size   host, >= every group's size
+ *   max_prefix_len   host, >= every prefix_len
+ *   workspace        device scratch of
+ *                    pa_decode_shared_prefix_workspace_size(...) bytes
+ *                    (no zeroing needed)
+ *   status           device int32, caller-zeroed, or NULL: PA_ERR_INVALID_ARG
+ *                    for inconsistent groups, prefixes or lengths,
+ *                    PA_ERR_DEVICE_TIMEOUT if a bounded wait expired
+ * Supported: bf16 K/V and q, head_dim 128, block_size 8..256, num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8, 16}; PA_ERR_UNSUPPORTED otherwise;
+ * PA_ERR_WORKSPACE if the workspace is too small.  Three launches on stream.
+ * ---------------------------------------------------------------------- */
+size_t    pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                 int32_t num_kv_heads, int32_t num_groups,
+                                                 int32_t max_group_size, int32_t max_prefix_len);
+pa_status pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q,
+                                  int32_t num_seqs, int32_t num_q_heads,
+                                  const void* k_cache, const void* v_cache, int32_t num_blocks,
+                                  int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                  pa_dtype dtype, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t max_context_len, const int32_t* group_start,
+                                  const int32_t* prefix_len, int32_t num_groups,
+                                  int32_t max_group_size, int32_t max_prefix_len, float scale,
+                                  int32_t* status, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------
  * Paged prefill attention -- [PA] "KV Cache 为什么难管理": the prefill phase
  * processes a prompt's tokens together; [PA] "Block Table 如何工作": every
  * token reads its sequence's K/V through the block table.  Chunked prefill

@@ -39,6 +39,9 @@ SIGNATURES = {
                                           i32, i32, vp]),
     "pa_copy_blocks_layers": (i32, [vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, i32, vp]),
     "pa_decode_workspace_size": (C.c_size_t, [i32, i32, i32, i32, i32, i32, i32, i32]),
+    "pa_decode_shared_prefix_workspace_size": (C.c_size_t, [i32, i32, i32, i32, i32, i32]),
+    "pa_decode_shared_prefix": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp,
+                                      i32, vp, vp, i32, i32, i32, C.c_float, vp, vp, C.c_size_t, vp]),
     "pa_prefill": (i32, [vp, i32, vp, i32, vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp,
                          i32, C.c_float, vp, vp]),
     "pa_decode": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32,

@@ -369,6 +369,31 @@ bool encode_q_tokens(CUtensorMap* m, const void* base, uint64_t tokens, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The tensor-core prefill kernel over `items` work items (any mode).
+pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void* q,
+                         const void* k_cache, const void* v_cache, int64_t cache_rows,
+                         void* stream) {
+  if (items >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+  if (items == 0) return PA_OK;
+  const void* fn = pa::prefill_umma_fn(G);
+  const int smem = pa::prefill_umma_smem_bytes();
+  int ctas = 0;
+  pa_status st = prepare_kernel(fn, 256, smem, &ctas);
+  if (st != PA_OK) return st;
+  if (ctas > items) ctas = static_cast<int>(items);
+  CUtensorMap tmq, tmk, tmv;
+  const uint32_t box_rows = static_cast<uint32_t>(p.block_size < 128 ? p.block_size : 128);
+  if (!encode_q_tokens(&tmq, q, static_cast<uint64_t>(p.num_tokens),
+                       static_cast<uint64_t>(p.num_q_heads) * 128, static_cast<uint32_t>(128 / G)) ||
+      !encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
+      !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows))
+    return PA_ERR_CUDA;
+  void* args[] = {&p, &tmq, &tmk, &tmv};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(256), args,
+                                   static_cast<size_t>(smem), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, int32_t num_tokens,
                      const int32_t* cu_q, const int32_t* q_start, int32_t num_seqs,
                      int32_t max_q_len, int32_t num_q_heads, const void* k_cache,
@@ -410,23 +435,110 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, int32_t num_t
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   const int64_t items = static_cast<int64_t>(num_seqs) * num_kv_heads * p.tiles_per_seq;
-  if (items >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
-  const void* fn = pa::prefill_umma_fn(G);
-  const int smem = pa::prefill_umma_smem_bytes();
-  int ctas = 0;
-  st = prepare_kernel(fn, 256, smem, &ctas);
+  return launch_prefill(p, G, items, q, k_cache, v_cache, cache_rows, stream);
+}
+
+// Shared-prefix decode: partition size of the groups' prefixes and the
+// partial-result scratch [partitions + 1][num_seqs * num_q_heads][2 + 128].
+namespace {
+int64_t cascade_part_tokens(int64_t max_prefix, int64_t items_per_part) {
+  // enough (prefix partition, tile, group, kv head) items for every SM twice,
+  // partitions of at least 256 keys, in 128-key multiples
+  int64_t parts = (2 * kSmCountHint + items_per_part - 1) / (items_per_part > 0 ? items_per_part : 1);
+  if (parts < 1) parts = 1;
+  int64_t pt = (max_prefix + parts - 1) / parts;
+  pt = round_up(pt < 256 ? 256 : pt, 128);
+  return pt;
+}
+}  // namespace
+
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t num_groups,
+                                              int32_t max_group_size, int32_t max_prefix_len) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_groups < 0 ||
+      max_group_size < 0 || max_prefix_len < 0 || num_q_heads % num_kv_heads)
+    return 0;
+  const int G = num_q_heads / num_kv_heads;
+  if (!pa::prefill_umma_fn(G)) return 0;
+  const int64_t tiles = (static_cast<int64_t>(max_group_size) + 128 / G - 1) / (128 / G);
+  const int64_t pt = cascade_part_tokens(max_prefix_len, static_cast<int64_t>(num_groups) * num_kv_heads * tiles);
+  const int64_t parts = (max_prefix_len + pt - 1) / pt;
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
+  return static_cast<size_t>((parts + 1) * rows * (2 + 128) * 4 + 256);
+}
+
+pa_status pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, int32_t num_seqs,
+                                  int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                  int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                  int32_t head_dim, pa_dtype dtype, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t max_context_len, const int32_t* group_start,
+                                  const int32_t* prefix_len, int32_t num_groups,
+                                  int32_t max_group_size, int32_t max_prefix_len, float scale,
+                                  int32_t* status, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
-  if (ctas > items) ctas = static_cast<int>(items);
-  CUtensorMap tmq, tmk, tmv;
-  const uint32_t box_rows = static_cast<uint32_t>(block_size < 128 ? block_size : 128);
-  if (!encode_q_tokens(&tmq, q, static_cast<uint64_t>(num_tokens),
-                       static_cast<uint64_t>(num_q_heads) * 128, static_cast<uint32_t>(TQ)) ||
-      !encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
-      !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows))
-    return PA_ERR_CUDA;
-  void* args[] = {&p, &tmq, &tmk, &tmv};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(256), args,
-                                   static_cast<size_t>(smem), static_cast<cudaStream_t>(stream));
+  if (num_seqs < 0 || num_q_heads <= 0 || num_groups < 0 || max_group_size < 0 ||
+      max_prefix_len < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || !(scale > 0.f) ||
+      dtype_bytes(out_dtype) == 0 || num_q_heads % num_kv_heads)
+    return PA_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if (dtype != PA_DTYPE_BF16 || head_dim != 128 || block_size < 8 || !pa::prefill_umma_fn(G))
+    return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (num_groups <= 0 || !out || !q || !k_cache || !v_cache || !block_tables || !context_lens ||
+      !group_start || !prefix_len || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace))
+    return PA_ERR_INVALID_ARG;
+  const size_t need = pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                             num_groups, max_group_size, max_prefix_len);
+  if (need == 0) return PA_ERR_UNSUPPORTED;
+  if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+  const int64_t cache_rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
+  if (cache_rows >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+  const int TQ = 128 / G;
+  const int64_t tiles = (static_cast<int64_t>(max_group_size) + TQ - 1) / TQ;
+  const int64_t pt = cascade_part_tokens(max_prefix_len, static_cast<int64_t>(num_groups) * num_kv_heads * tiles);
+  const int64_t parts = (max_prefix_len + pt - 1) / pt;
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
+  pa::PrefillParams p{};
+  p.out = out;
+  p.out_bf16 = out_dtype == PA_DTYPE_BF16 ? 1 : 0;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.num_tokens = num_seqs;  // the queries are one row per sequence: q [num_seqs][H][128]
+  p.tiles_per_seq = static_cast<int32_t>(tiles);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  p.group_start = group_start;
+  p.prefix_len = prefix_len;
+  p.context_lens = context_lens;
+  p.num_groups = num_groups;
+  p.max_context_len = max_context_len;
+  p.part_tokens = static_cast<int32_t>(pt);
+  p.num_parts = static_cast<int32_t>(parts);
+  p.part_ml = static_cast<float*>(workspace);
+  p.part_o = p.part_ml + (parts + 1) * rows * 2;
+  // 1: the groups' prefixes, every member's queries against each prefix block once
+  p.mode = 1;
+  st = launch_prefill(p, G, parts * num_groups * num_kv_heads * tiles, q, k_cache, v_cache,
+                      cache_rows, stream);
+  if (st != PA_OK) return st;
+  // 2: every member's own tokens past its group's prefix
+  p.mode = 2;
+  st = launch_prefill(p, G, static_cast<int64_t>(num_seqs) * num_kv_heads, q, k_cache, v_cache,
+                      cache_rows, stream);
+  if (st != PA_OK) return st;
+  // 3: log-sum-exp merge into out
+  cudaError_t e = pa::launch_cascade_merge(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

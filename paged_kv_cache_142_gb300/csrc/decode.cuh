@@ -87,9 +87,22 @@ struct PrefillParams {
   int32_t tiles_per_seq;   // ceil(max chunk length / tokens per tile)
   float scale_log2;
   int32_t* status;         // device error word (may be null)
+  // shared-prefix decode (mode 1: the groups' prefixes, mode 2: the members'
+  // own tokens past them); mode 0 is causal prefill
+  int32_t mode;
+  const int32_t* group_start;   // [num_groups + 1] member ranges of the batch
+  const int32_t* prefix_len;    // [num_groups] shared tokens (whole blocks)
+  const int32_t* context_lens;  // [num_seqs]
+  int32_t num_groups;
+  int32_t max_context_len;
+  int32_t part_tokens;          // keys per prefix partition (multiple of 128)
+  int32_t num_parts;            // prefix partitions per group (max); the suffix is slot num_parts
+  float* part_ml;               // [num_parts + 1][num_seqs * num_q_heads][2]: max (log2), sum
+  float* part_o;                // [num_parts + 1][num_seqs * num_q_heads][128]: unnormalised O
 };
 const void* prefill_umma_fn(int group);
 int prefill_umma_smem_bytes();
+cudaError_t launch_cascade_merge(const PrefillParams& p, cudaStream_t stream);
 
 // Cache ops over num_layers layers of one pool (layer strides in bytes,
 // multiples of 16); one layer is num_layers == 1.

@@ -66,31 +66,104 @@ constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEm
               kNumBars = 18;
 
 struct Item {
-  int seq, kvh, qb, tok0, ntq, pos0, kend, ntiles;
+  int seq, kvh, qb, tok0, ntq, pos0, k_start, kend, ntiles, trow_seq, causal, part;
 };
 
+// The group of batch sequence i (group_start is non-decreasing).
+__device__ __forceinline__ int group_of(const PrefillParams& p, int i) {
+  int lo = 0, hi = p.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.group_start[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void bad_input(const PrefillParams& p) {
+  if (p.status) atomicExch(p.status, kDevErrInvalidArg);
+}
+
+// Work item w.  Mode 0 (prefill): (tile of TQ tokens, sequence, kv head),
+// later tiles first, causal keys [0, position].  Mode 1 (shared prefix):
+// (prefix partition, tile of TQ members, group, kv head) over the group's
+// prefix keys, read through its first member's table.  Mode 2 (own tokens):
+// (member, kv head) over keys [prefix, len) of the member's table.
 __device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, Item& it) {
   const int hkv = p.num_kv_heads;
-  const int per_tile = p.num_seqs * hkv;
-  const int tile = p.tiles_per_seq - 1 - w / per_tile;
-  const int rem = w - (w / per_tile) * per_tile;
-  it.seq = rem / hkv;
-  it.kvh = rem - it.seq * hkv;
   const int TQ = 128 / G;
-  it.qb = p.cu_q[it.seq];
-  const int n = p.cu_q[it.seq + 1] - it.qb;
-  it.tok0 = tile * TQ;
-  if (n <= 0 || it.tok0 >= n) return false;  // no tokens in this tile
-  const int q0 = p.q_start[it.seq];
-  if (it.qb < 0 || it.qb + n > p.num_tokens || q0 < 0 ||
-      static_cast<int64_t>(q0) + n > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
-    if (p.status) atomicExch(p.status, kDevErrInvalidArg);  // offsets outside q or the table
-    return false;
+  const int64_t table_tokens = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
+  if (p.mode == 0) {
+    const int per_tile = p.num_seqs * hkv;
+    const int tile = p.tiles_per_seq - 1 - w / per_tile;
+    const int rem = w - (w / per_tile) * per_tile;
+    it.seq = rem / hkv;
+    it.kvh = rem - it.seq * hkv;
+    it.qb = p.cu_q[it.seq];
+    const int n = p.cu_q[it.seq + 1] - it.qb;
+    it.tok0 = tile * TQ;
+    if (n <= 0 || it.tok0 >= n) return false;  // no tokens in this tile
+    const int q0 = p.q_start[it.seq];
+    if (it.qb < 0 || it.qb + n > p.num_tokens || q0 < 0 || static_cast<int64_t>(q0) + n > table_tokens) {
+      bad_input(p);  // offsets outside q or the table
+      return false;
+    }
+    it.ntq = min(TQ, n - it.tok0);
+    it.pos0 = q0 + it.tok0;
+    it.k_start = 0;
+    it.kend = it.pos0 + it.ntq;
+    it.trow_seq = it.seq;
+    it.causal = 1;
+    it.part = 0;
+  } else if (p.mode == 1) {
+    const int per_part = p.num_groups * hkv * p.tiles_per_seq;
+    it.part = w / per_part;
+    const int rem = w - it.part * per_part;
+    const int tile = rem / (p.num_groups * hkv);
+    const int r2 = rem - tile * (p.num_groups * hkv);
+    const int grp = r2 / hkv;
+    it.kvh = r2 - grp * hkv;
+    it.seq = grp;
+    it.qb = p.group_start[grp];
+    const int n = p.group_start[grp + 1] - it.qb;
+    it.tok0 = tile * TQ;
+    if (n <= 0 || it.tok0 >= n) return false;
+    const int P = p.prefix_len[grp];
+    if (it.qb < 0 || it.qb + n > p.num_seqs || P < 0 || P % p.block_size != 0 || P > table_tokens) {
+      bad_input(p);
+      return false;
+    }
+    it.k_start = it.part * p.part_tokens;
+    it.kend = min(P, it.k_start + p.part_tokens);
+    if (it.k_start >= it.kend) return false;  // the group's prefix has fewer partitions
+    it.ntq = min(TQ, n - it.tok0);
+    it.pos0 = 0;
+    it.trow_seq = it.qb;  // the prefix blocks are the same in every member's table
+    it.causal = 0;
+  } else {
+    const int i = w / hkv;
+    it.kvh = w - i * hkv;
+    it.seq = i;
+    it.qb = i;
+    it.tok0 = 0;
+    it.ntq = 1;
+    it.pos0 = 0;
+    const int grp = group_of(p, i);
+    const int P = p.prefix_len[grp];
+    const int len = p.context_lens[i];
+    if (len < 0 || len > p.max_context_len || static_cast<int64_t>(len) > table_tokens || P < 0 ||
+        P % p.block_size != 0 || P > len) {
+      bad_input(p);
+      return false;
+    }
+    it.k_start = P;
+    it.kend = len;
+    if (it.kend <= it.k_start) return false;  // no own tokens: the merge skips this part
+    it.trow_seq = i;
+    it.causal = 0;
+    it.part = p.num_parts;
   }
-  it.ntq = min(TQ, n - it.tok0);
-  it.pos0 = q0 + it.tok0;
-  it.kend = it.pos0 + it.ntq;
-  it.ntiles = (it.kend + 127) / 128;
+  it.ntiles = (it.kend - it.k_start + 127) / 128;
   return true;
 }
 
@@ -129,7 +202,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hkv = p.num_kv_heads, bs = p.block_size;
   const int bs_log = __ffs(bs) - 1;
-  const int items = p.num_seqs * hkv * p.tiles_per_seq;
+  const int items = p.mode == 0   ? p.num_seqs * hkv * p.tiles_per_seq
+                    : p.mode == 1 ? p.num_parts * p.num_groups * hkv * p.tiles_per_seq
+                                  : p.num_seqs * hkv;
 
   if (tid == 0) {
     ptx::mbar_init(&bars[kQFull], 1);
@@ -184,15 +259,15 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
             ptx::tma_load_2d(qbuf + h * 16384 + g * TQ * 128, &tm_q, (it.kvh * G + g) * 128 + h * 64,
                              it.qb + it.tok0, &bars[kQFull], pol_q);
       }
-      const int32_t* trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(it.trow_seq) * p.max_blocks_per_seq;
       for (int t = 0; t < it.ntiles && !aborted; ++t, ++fc) {
         const int slot = static_cast<int>(fc & 1u);
         const uint32_t ph = (fc >> 1) & 1u;
-        const int nv = min(128, it.kend - t * 128);
+        const int nv = min(128, it.kend - it.k_start - t * 128);
         const int nbox = (nv + box_rows - 1) / box_rows;
         int row = 0;
         if (lane < nbox) {
-          const int tok = t * 128 + lane * box_rows;
+          const int tok = it.k_start + t * 128 + lane * box_rows;
           const int lb = tok >> bs_log;
           int phys = trow[lb];
           if (phys < 0 || phys >= p.num_blocks) {  // never read outside the pool
@@ -227,7 +302,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
-      const int nv = min(128, it.kend - t * 128);
+      const int nv = min(128, it.kend - it.k_start - t * 128);
       const int nks = (nv + 15) / 16;
       if (!aborted && (nv & 15)) {  // V rows past the end inside the last 16-key step
         const int nrows = nks * 16 - nv;
@@ -315,7 +390,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       Item it;
       if (!item_at(p, w, G, it)) continue;
       const bool valid = trow < it.ntq;
-      const int limit = valid ? it.pos0 + trow + 1 : 0;  // keys visible to this row
+      // keys visible to this row: its causal position, or the whole range
+      const int limit = !valid ? 0 : (it.causal ? it.pos0 + trow + 1 : it.kend);
       float m_ref = -CUDART_INF_F, l = 0.f;
       for (int t = 0; t < it.ntiles; ++t) {
         const int b = static_cast<int>(sc & 1u);
@@ -324,7 +400,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         if (aborted) break;
         ptx::tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * 128;
-        const int key0 = t * 128;
+        const int key0 = it.k_start + t * 128;
         // pass 1: the row's max over this tile
         float mt = -CUDART_INF_F;
 #pragma unroll 1
@@ -408,14 +484,27 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       aborted = __any_sync(0xffffffffu, aborted);
       if (aborted) break;
       ptx::tc_fence_after();
-      const float inv = valid && l > 0.f ? 1.f / l : 0.f;
-      const int64_t orow = (static_cast<int64_t>(it.qb + it.tok0 + trow) * p.num_q_heads + it.kvh * G + g) * 128;
+      const bool partial = p.mode != 0;  // shared-prefix decode: (max, sum, unnormalised O)
+      const float inv = partial ? 1.f : (valid && l > 0.f ? 1.f / l : 0.f);
+      const int64_t prow = static_cast<int64_t>(it.qb + it.tok0 + trow) * p.num_q_heads + it.kvh * G + g;
+      const int64_t orow = prow * 128;
+      const int64_t slot_rows = static_cast<int64_t>(it.part) * p.num_seqs * p.num_q_heads;
+      if (partial && valid) {
+        p.part_ml[(slot_rows + prow) * 2] = m_ref;
+        p.part_ml[(slot_rows + prow) * 2 + 1] = l;
+      }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         ptx::TmemLd<32>::run(tmem + lane_base + 256 + c * 32, v);
         ptx::tmem_wait_ld();
-        if (valid) {
+        if (valid && partial) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + (slot_rows + prow) * 128 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        } else if (valid) {
           if (p.out_bf16) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c * 32);
 #pragma unroll
@@ -448,6 +537,49 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, 512);
   if (tid == 0 && flags[0] && p.status) atomicExch(p.status, kDevErrTimeout);
+}
+
+// Shared-prefix decode, last step: for each (member, q head), the prefix
+// partitions' and the own tokens' (max, sum, O) merged by log-sum-exp.
+__global__ void __launch_bounds__(128) cascade_merge_kernel(const __grid_constant__ PrefillParams p) {
+  const int rows = p.num_seqs * p.num_q_heads;
+  const int row = blockIdx.x;  // member * H + head
+  if (row >= rows) return;
+  const int i = row / p.num_q_heads;
+  const int d = threadIdx.x;
+  const int grp = prefill_detail::group_of(p, i);
+  const int P = max(0, p.prefix_len[grp]);
+  const int len = p.context_lens[i];
+  if (len < P && d == 0) prefill_detail::bad_input(p);  // a member shorter than its group's prefix
+  const int nparts = (P + p.part_tokens - 1) / p.part_tokens;
+  float M = -CUDART_INF_F;
+  for (int k = 0; k < nparts; ++k) M = fmaxf(M, p.part_ml[(static_cast<int64_t>(k) * rows + row) * 2]);
+  const bool own = len > P;
+  const int64_t srow = static_cast<int64_t>(p.num_parts) * rows + row;
+  if (own) M = fmaxf(M, p.part_ml[srow * 2]);
+  float L = 0.f, O = 0.f;
+  for (int k = 0; k < nparts; ++k) {
+    const int64_t r = static_cast<int64_t>(k) * rows + row;
+    const float wk = exp2f(p.part_ml[r * 2] - M);
+    L = fmaf(wk, p.part_ml[r * 2 + 1], L);
+    O = fmaf(wk, p.part_o[r * 128 + d], O);
+  }
+  if (own) {
+    const float ws = exp2f(p.part_ml[srow * 2] - M);
+    L = fmaf(ws, p.part_ml[srow * 2 + 1], L);
+    O = fmaf(ws, p.part_o[srow * 128 + d], O);
+  }
+  const float v = L > 0.f ? O / L : 0.f;  // a sequence with no tokens gives zeros
+  const int64_t idx = static_cast<int64_t>(row) * 128 + d;
+  if (p.out_bf16) static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+  else static_cast<float*>(p.out)[idx] = v;
+}
+
+cudaError_t launch_cascade_merge(const PrefillParams& p, cudaStream_t stream) {
+  const int rows = p.num_seqs * p.num_q_heads;
+  if (rows == 0) return cudaSuccess;
+  cascade_merge_kernel<<<rows, 128, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 const void* prefill_umma_fn(int group) {

@@ -141,6 +141,34 @@ def pa_prefill(out, q, k_cache, v_cache, cu_q, q_start, block_tables, scale, num
             "pa_prefill")
 
 
+def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                            max_context_len, group_start, prefix_len, max_group_size, max_prefix_len,
+                            workspace=None, status=None, stream=None):
+    """Decode with each group's shared prefix read once for all its members
+    (groups of consecutive sequences; see pa_decode_shared_prefix).  Returns
+    the workspace it used (allocated here when not given)."""
+    NB, Hkv, bs, D = _cache_dims(k_cache, v_cache)
+    _need(Hkv == num_kv_heads, "num_kv_heads does not match the cache")
+    B, H, Dq = q.shape
+    _need(Dq == D and out.shape == q.shape and q.is_contiguous() and out.is_contiguous(), "q/out [B, H, D]")
+    Gn = prefix_len.numel()
+    _need(group_start.dtype == torch.int32 and prefix_len.dtype == torch.int32 and group_start.numel() == Gn + 1,
+          "group_start [G+1] and prefix_len [G] must be int32")
+    need = _LIB.pa_decode_shared_prefix_workspace_size(B, H, Hkv, Gn, int(max_group_size), int(max_prefix_len))
+    if need == 0:
+        raise PAError(L.PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    L.check(_LIB.pa_decode_shared_prefix(
+        out.data_ptr(), dtype_code(out.dtype), q.data_ptr(), B, H, k_cache.data_ptr(), v_cache.data_ptr(),
+        NB, bs, Hkv, D, dtype_code(k_cache.dtype), block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), int(max_context_len), group_start.data_ptr(), prefix_len.data_ptr(), Gn,
+        int(max_group_size), int(max_prefix_len), float(scale),
+        status.data_ptr() if status is not None else None, workspace.data_ptr(), workspace.numel(),
+        _stream(stream)), "pa_decode_shared_prefix")
+    return workspace
+
+
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                              max_context_len, partition_tokens=0) -> int:
     n = _LIB.pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
