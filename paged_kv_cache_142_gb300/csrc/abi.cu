@@ -52,6 +52,7 @@ pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_
 // Tensor-core kernel layout constants (must match decode_umma.cuh).
 constexpr int kUmmaThreadsHost = 448;
 constexpr int kUmmaTileBytesHost = 32768;
+constexpr int kPrefillThreads = 288;  // must match the prefill kernel
 
 struct Plan {
   DecodeKernelInfo info;
@@ -378,7 +379,7 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
   const void* fn = pa::prefill_umma_fn(G);
   const int smem = pa::prefill_umma_smem_bytes();
   int ctas = 0;
-  pa_status st = prepare_kernel(fn, 256, smem, &ctas);
+  pa_status st = prepare_kernel(fn, kPrefillThreads, smem, &ctas);
   if (st != PA_OK) return st;
   if (ctas > items) ctas = static_cast<int>(items);
   CUtensorMap tmq, tmk, tmv;
@@ -389,7 +390,7 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
       !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows))
     return PA_ERR_CUDA;
   void* args[] = {&p, &tmq, &tmk, &tmv};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(256), args,
+  cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(kPrefillThreads), args,
                                    static_cast<size_t>(smem), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -19,16 +19,20 @@
 // bf16 hi = bf16(p) and lo = bf16(p - hi), two passes of eight MMAs, so each
 // probability keeps about 16 bits.
 //
-// One CTA per SM, 256 threads, persistent over (tile of TQ tokens, sequence,
+// One CTA per SM, 288 threads, persistent over (tile of TQ tokens, sequence,
 // kv head) items, later (longer) tiles first:
 //  * warp 0 loads the item's query rows (2-D TMA boxes, one per head and
 //    64-dim half) and its K tiles (one 4-D TMA box per block, as in decode)
 //    into a 2-stage ring; warp 2 loads the V tiles likewise;
-//  * warp 1 issues Q.K^T of tile t, then P.V of tile t - 1 (so the softmax
-//    of tile t overlaps the products), zeroing first the V rows past the end
-//    inside the last 16-key step of the item's last tile;
+//  * warp 1 issues Q.K^T of every tile as soon as its K tile has landed and
+//    an S buffer is free (so the softmax of tile t overlaps Q.K^T of t + 1);
+//  * warps 3 and 8 issue P.V of the hi and the lo halves of P into two O
+//    accumulators in parallel (one thread issues an MMA about every hundred
+//    cycles), warp 3 zeroing first the V rows past the end inside the last
+//    16-key step of the item's last tile;
 //  * warps 4-7 own tensor-memory lanes 0-127, one query row per thread: per
-//    tile they read the row of S twice (max, then exponentials), mask keys
+//    tile they load the row of S into registers at once (max, then
+//    exponentials from the same registers), mask keys
 //    past the row's position, run the online softmax in fp32 (log2 domain)
 //    and write P hi/lo to shared memory (128-byte swizzle, K-major).  The
 //    running max is the reference of P and O and is raised only when a row's
@@ -49,7 +53,7 @@ namespace pa {
 
 namespace prefill_detail {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;  // 9 warps
 constexpr int kTileBytes = 32768;
 constexpr int kOffQ = 0;
 constexpr int kOffPhi = 32768;
@@ -63,7 +67,8 @@ constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only pa
 // barriers
 constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
               kSFull = 10, kSEmpty = 12, kPFull = 14, kPVDone = 15, kOEmpty = 16, kDrain = 17,
-              kNumBars = 18;
+              kVZero = 20, kNumBars = 21;  // drains: Q.K^T, P.V hi, P.V lo; then V-tail zeroed
+constexpr uint32_t kColO = 256;  // O from the hi halves of P; the lo halves' O at kColO + 128
 
 struct Item {
   int seq, kvh, qb, tok0, ntq, pos0, k_start, kend, ntiles, trow_seq, causal, part;
@@ -171,6 +176,14 @@ __device__ __forceinline__ void wait(uint64_t* bar, uint32_t parity, bool& abort
   if (!aborted && !ptx::mbar_wait(bar, parity, kWaitLimitNs)) aborted = true;
 }
 
+// 2^x by the ex2.approx.ftz instruction (relative error about 2^-22; very
+// negative x gives 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -213,19 +226,20 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       ptx::mbar_init(&bars[kKFull + s], 1);
       ptx::mbar_init(&bars[kKEmpty + s], 1);
       ptx::mbar_init(&bars[kVFull + s], 1);
-      ptx::mbar_init(&bars[kVEmpty + s], 1);
+      ptx::mbar_init(&bars[kVEmpty + s], 2);  // both P.V warps
       ptx::mbar_init(&bars[kSFull + s], 1);
       ptx::mbar_init(&bars[kSEmpty + s], 4);
     }
     ptx::mbar_init(&bars[kPFull], 4);
-    ptx::mbar_init(&bars[kPVDone], 1);
+    ptx::mbar_init(&bars[kPVDone], 2);  // both P.V warps
     ptx::mbar_init(&bars[kOEmpty], 4);
-    ptx::mbar_init(&bars[kDrain], 1);
+    for (int d = 0; d < 3; ++d) ptx::mbar_init(&bars[kDrain + d], 1);
+    ptx::mbar_init(&bars[kVZero], 1);
     flags[0] = 0;
     ptx::mbar_init_fence();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, 512);  // S[2] x 128 columns, then O x 128
+    ptx::tmem_alloc(tmem_slot, 512);  // S[2] x 128 columns, then O (hi, lo) x 128
     ptx::tc_fence_before();
   }
   __syncthreads();
@@ -289,81 +303,36 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       ++ic;
     }
   } else if (warp == 1) {
-    // ============================ MMA issue ============================
+    // ============================ Q.K^T issue ============================
     constexpr uint32_t kIdQK = ptx::idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, 128, 0, 1);
-    uint32_t ic = 0, kc = 0, vc = 0, sc = 0, tc = 0;
-    auto pv = [&](const Item& it, int t) {
-      const int vslot = static_cast<int>(vc & 1u);
-      unsigned char* vt = vring + vslot * kTileBytes;
-      if (lane == 0) {
-        wait(&bars[kVFull + vslot], (vc >> 1) & 1u, aborted);
-        wait(&bars[kPFull], tc & 1u, aborted);
-        if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
-      }
-      aborted = __shfl_sync(0xffffffffu, aborted, 0);
-      const int nv = min(128, it.kend - it.k_start - t * 128);
-      const int nks = (nv + 15) / 16;
-      if (!aborted && (nv & 15)) {  // V rows past the end inside the last 16-key step
-        const int nrows = nks * 16 - nv;
-        for (int c = lane; c < nrows * 16; c += 32) {
-          const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
-          *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        ptx::fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (!aborted && lane == 0) {
-        ptx::tc_fence_after();
-        const uint32_t od = tmem + 256;
-        for (int ks = 0; ks < nks; ++ks) {
-          const uint64_t bd = ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128);
-          const int a_off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          ptx::umma_bf16(od, ptx::smem_desc(phi + a_off, 16, 1024, ptx::kLayoutSw128), bd, kIdPV,
-                         t > 0 || ks > 0);
-          ptx::umma_bf16(od, ptx::smem_desc(plo + a_off, 16, 1024, ptx::kLayoutSw128), bd, kIdPV, 1);
-        }
-        ptx::umma_commit(&bars[kPVDone]);
-        ptx::umma_commit(&bars[kVEmpty + vslot]);
-      }
-      __syncwarp();
-      ++vc;
-      ++tc;
-    };
+    uint32_t ic = 0, kc = 0, sc = 0;
     for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
       Item it;
       if (!item_at(p, w, G, it)) continue;
-      if (lane == 0) wait(&bars[kQFull], ic & 1u, aborted);
-      for (int t = 0; t < it.ntiles; ++t) {
-        const int b = static_cast<int>(sc & 1u);
-        const int kslot = static_cast<int>(kc & 1u);
-        if (lane == 0) {
+      if (lane == 0) {
+        wait(&bars[kQFull], ic & 1u, aborted);
+        for (int t = 0; t < it.ntiles && !aborted; ++t, ++kc, ++sc) {
+          const int b = static_cast<int>(sc & 1u);
+          const int kslot = static_cast<int>(kc & 1u);
           wait(&bars[kKFull + kslot], (kc >> 1) & 1u, aborted);
           wait(&bars[kSEmpty + b], ((sc >> 1) & 1u) ^ 1u, aborted);
-          if (!aborted) {
-            ptx::tc_fence_after();
-            const unsigned char* kt = kring + kslot * kTileBytes;
-            const uint32_t sd = tmem + b * 128;
+          if (aborted) break;
+          ptx::tc_fence_after();
+          const unsigned char* kt = kring + kslot * kTileBytes;
+          const uint32_t sd = tmem + b * 128;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const int h = kk >> 2, k4 = kk & 3;
-              ptx::umma_bf16(sd, ptx::smem_desc(qbuf + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
-                             ptx::smem_desc(kt + h * 1024 + k4 * 32, 16, 2048, ptx::kLayoutSw128), kIdQK,
-                             kk > 0);
-            }
-            ptx::umma_commit(&bars[kSFull + b]);
-            ptx::umma_commit(&bars[kKEmpty + kslot]);
-            if (t == it.ntiles - 1) ptx::umma_commit(&bars[kQEmpty]);
+          for (int kk = 0; kk < 8; ++kk) {
+            const int h = kk >> 2, k4 = kk & 3;
+            ptx::umma_bf16(sd, ptx::smem_desc(qbuf + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
+                           ptx::smem_desc(kt + h * 1024 + k4 * 32, 16, 2048, ptx::kLayoutSw128), kIdQK,
+                           kk > 0);
           }
+          ptx::umma_commit(&bars[kSFull + b]);
+          ptx::umma_commit(&bars[kKEmpty + kslot]);
+          if (t == it.ntiles - 1) ptx::umma_commit(&bars[kQEmpty]);
         }
-        aborted = __shfl_sync(0xffffffffu, aborted, 0);
-        ++kc;
-        ++sc;
-        if (aborted) break;
-        if (t > 0) pv(it, t - 1);
       }
-      if (!aborted) pv(it, it.ntiles - 1);
+      aborted = __shfl_sync(0xffffffffu, aborted, 0);
       ++ic;
     }
     if (lane == 0) {  // nothing may be in flight when tensor memory is freed
@@ -373,7 +342,69 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       if (aborted || drain_aborted) flags[0] = 1;
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp == 3 || warp == 8) {
+    // ============ P.V issue: warp 3 the hi halves of P, warp 8 the lo ============
+    // Each accumulates into its own O (columns kColO / kColO + 128), so the
+    // two chains issue in parallel; the epilogue adds them.
+    constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, 128, 0, 1);
+    const bool lo = warp == 8;
+    const unsigned char* pbase = lo ? plo : phi;
+    const uint32_t od = tmem + kColO + (lo ? 128u : 0u);
+    uint32_t ic = 0, vc = 0, tc = 0, zc = 0;
+    for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
+      Item it;
+      if (!item_at(p, w, G, it)) continue;
+      for (int t = 0; t < it.ntiles; ++t, ++vc, ++tc) {
+        const int vslot = static_cast<int>(vc & 1u);
+        unsigned char* vt = vring + vslot * kTileBytes;
+        if (lane == 0) {
+          wait(&bars[kVFull + vslot], (vc >> 1) & 1u, aborted);
+          wait(&bars[kPFull], tc & 1u, aborted);
+          if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        if (aborted) break;
+        const int nv = min(128, it.kend - it.k_start - t * 128);
+        const int nks = (nv + 15) / 16;
+        if (nv & 15) {  // V rows past the end inside the last 16-key step: zeroed by warp 3
+          if (!lo) {
+            const int nrows = nks * 16 - nv;
+            for (int c = lane; c < nrows * 16; c += 32) {
+              const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+              *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars[kVZero]);
+          } else {
+            if (lane == 0) wait(&bars[kVZero], zc & 1u, aborted);  // warp 3 has zeroed the rows
+            aborted = __shfl_sync(0xffffffffu, aborted, 0);
+          }
+          ++zc;
+          if (aborted) break;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tc_fence_after();
+          for (int ks = 0; ks < nks; ++ks)
+            ptx::umma_bf16(od, ptx::smem_desc(pbase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, ptx::kLayoutSw128),
+                           ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128), kIdPV, t > 0 || ks > 0);
+          ptx::umma_commit(&bars[kPVDone]);
+          ptx::umma_commit(&bars[kVEmpty + vslot]);
+        }
+        __syncwarp();
+      }
+      ++ic;
+    }
+    if (lane == 0) {
+      ptx::umma_commit(&bars[kDrain + (lo ? 2 : 1)]);
+      bool drain_aborted = false;
+      wait(&bars[kDrain + (lo ? 2 : 1)], 0, drain_aborted);
+      if (aborted || drain_aborted) flags[0] = 1;
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
     // ============ softmax / epilogue: one query row per thread ============
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;
@@ -385,6 +416,52 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
     // K-major [2 halves][128 rows][128 B] tile
     auto chunk_addr = [&](unsigned char* base, int c) -> unsigned char* {
       return base + (c >> 3) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
+    };
+    // max of the first n (<= 32, may be <= 0) raw scores of a 32-column chunk
+    auto chunk_max = [](const uint32_t (&v)[32], int n) -> float {
+      float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, m2 = -CUDART_INF_F, m3 = -CUDART_INF_F;
+      if (n >= 32) {  // the common case: no mask
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          m0 = fmaxf(m0, __uint_as_float(v[j]));
+          m1 = fmaxf(m1, __uint_as_float(v[j + 1]));
+          m2 = fmaxf(m2, __uint_as_float(v[j + 2]));
+          m3 = fmaxf(m3, __uint_as_float(v[j + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          m0 = j < n ? fmaxf(m0, __uint_as_float(v[j])) : m0;
+      }
+      return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+    };
+    // p for the chunk's columns (0 past the first n), added to the four
+    // partial sums, and its P hi/lo row pieces.  hi = p with its low 16 bits
+    // cleared (a bf16 value, exact), lo = the exact fp32 remainder cut the
+    // same way: |p - hi - lo| < 2^-16 p, both packed by bit moves
+    auto write_p = [&](const uint32_t (&v)[32], int c, int n, float neg_m, float (&ls)[4]) {
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        uint32_t hb[2], lb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float pr = fast_exp2(fmaf(__uint_as_float(v[j + e]), sl2, neg_m));
+          if (n < 32) pr = j + e < n ? pr : 0.f;
+          ls[(j + e) & 3] += pr;
+          hb[e] = __float_as_uint(pr) & 0xffff0000u;
+          lb[e] = __float_as_uint(pr - __uint_as_float(hb[e]));
+        }
+        hi[j >> 1] = __byte_perm(hb[0], hb[1], 0x7632);  // high halves: element 0 low, 1 high
+        lo[j >> 1] = __byte_perm(lb[0], lb[1], 0x7632);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        *reinterpret_cast<uint4*>(chunk_addr(phi, c * 4 + q)) =
+            make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+        *reinterpret_cast<uint4*>(chunk_addr(plo, c * 4 + q)) =
+            make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+      }
     };
     for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
       Item it;
@@ -401,17 +478,21 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * 128;
         const int key0 = it.k_start + t * 128;
-        // pass 1: the row's max over this tile
-        float mt = -CUDART_INF_F;
+        // keys of this tile visible to the row: a prefix of nvis columns
+        const int nvis = min(128, max(0, limit - key0));
+        // pass 1: the row's max over its visible raw scores (scale > 0 keeps
+        // the order), two 32-column chunks per tensor-memory wait
+        float mraw = -CUDART_INF_F;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          ptx::TmemLd<32>::run(sbase + c * 32, v);
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t va[32], vb[32];
+          ptx::TmemLd<32>::run(sbase + c * 32, va);
+          ptx::TmemLd<32>::run(sbase + c * 32 + 32, vb);
           ptx::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (key0 + c * 32 + j < limit) mt = fmaxf(mt, __uint_as_float(v[j]) * sl2);
+          mraw = fmaxf(mraw, chunk_max(va, nvis - c * 32));
+          mraw = fmaxf(mraw, chunk_max(vb, nvis - c * 32 - 32));
         }
+        const float mt = mraw * sl2;
         // P and O are free once the previous tile's P.V is done
         if (t > 0) {
           wait(&bars[kPVDone], (tc - 1) & 1u, aborted);
@@ -427,54 +508,41 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           m_ref = mn;
           l *= alpha;
         }
-        if (__any_sync(0xffffffffu, rescale)) {  // warp-collective O rescale in tensor memory
+        if (__any_sync(0xffffffffu, rescale)) {  // warp-collective rescale of both O in tensor memory
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint32_t v[32];
-            ptx::TmemLd<32>::run(tmem + lane_base + 256 + c * 32, v);
+            ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            ptx::tmem_st32(tmem + lane_base + 256 + c * 32, v);
+            ptx::tmem_st32(tmem + lane_base + kColO + c * 32, v);
           }
           ptx::tmem_wait_st();
         }
-        // pass 2: p = 2^(s - m_ref) (0 for masked keys), row sum, P hi/lo rows
+        // pass 2: p = 2^(s * scale_log2 - m_ref) (0 for masked keys), row sum,
+        // P hi/lo rows; S is free once its last chunk is loaded
+        const float neg_m = -m_ref;
+        float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          ptx::TmemLd<32>::run(sbase + c * 32, v);
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t va[32], vb[32];
+          ptx::TmemLd<32>::run(sbase + c * 32, va);
+          ptx::TmemLd<32>::run(sbase + c * 32 + 32, vb);
           ptx::tmem_wait_ld();
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float pr[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const bool vis = key0 + c * 32 + j + e < limit;
-              pr[e] = vis ? exp2f(__uint_as_float(v[j + e]) * sl2 - m_ref) : 0.f;
-              l += pr[e];
-            }
-            const float h0 = __bfloat162float(__float2bfloat16_rn(pr[0]));
-            const float h1 = __bfloat162float(__float2bfloat16_rn(pr[1]));
-            hi[j >> 1] = pack_bf16(h0, h1);
-            lo[j >> 1] = pack_bf16(pr[0] - h0, pr[1] - h1);
+          if (c == 2) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars[kSEmpty + b]);
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            *reinterpret_cast<uint4*>(chunk_addr(phi, c * 4 + q)) =
-                make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-            *reinterpret_cast<uint4*>(chunk_addr(plo, c * 4 + q)) =
-                make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-          }
+          write_p(va, c, nvis - c * 32, neg_m, lsum);
+          write_p(vb, c + 1, nvis - c * 32 - 32, neg_m, lsum);
         }
+        l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
         ptx::tc_fence_before();
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(&bars[kSEmpty + b]);
-          ptx::mbar_arrive(&bars[kPFull]);
-        }
+        if (lane == 0) ptx::mbar_arrive(&bars[kPFull]);
         ++sc;
         ++tc;
       }
@@ -495,9 +563,12 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        ptx::TmemLd<32>::run(tmem + lane_base + 256 + c * 32, v);
+        uint32_t v[32], vl[32];
+        ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
+        ptx::TmemLd<32>::run(tmem + lane_base + kColO + 128 + c * 32, vl);
         ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
         if (valid && partial) {
           float4* dst = reinterpret_cast<float4*>(p.part_o + (slot_rows + prow) * 128 + c * 32);
 #pragma unroll
