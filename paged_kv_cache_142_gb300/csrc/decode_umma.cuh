@@ -346,6 +346,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 2^x by the ex2.approx.ftz instruction (relative error about 2^-22; -inf
+// and very negative x give 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace umma_detail
 
 template <int G>
@@ -746,8 +754,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
         for (int k = 1; k < 4; ++k) mt = fmaxf(mt, red_m[(b * 4 + k) * 16 + g]);
         const float mn = fmaxf(m_run[g], mt);
-        al[g] = exp2f(m_run[g] - mn);
-        pr[g] = valid ? exp2f(s[g] - mn) : 0.f;
+        al[g] = fast_exp2(m_run[g] - mn);
+        pr[g] = valid ? fast_exp2(s[g] - mn) : 0.f;
         l_thr[g] = l_thr[g] * al[g] + pr[g];
         m_run[g] = mn;
       }
@@ -767,20 +775,22 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           }
         }
       }
-      // P row r: columns [0, LO) hold bf16(p) of heads 0..G-1, columns
-      // [LO, NP) the bf16 remainder p - bf16(p); unused heads are zero
-      float pc[NP];
+      // P row r: columns [0, LO) hold hi = p with its low 16 bits cleared
+      // (a bf16 value, exact) for heads 0..G-1, columns [LO, NP) the exact
+      // fp32 remainder p - hi cut the same way (|p - hi - lo| < 2^-16 p),
+      // as bf16 bit patterns; unused heads are zero
+      uint32_t pc[NP];
 #pragma unroll
-      for (int c = 0; c < NP; ++c) pc[c] = 0.f;
+      for (int c = 0; c < NP; ++c) pc[c] = 0u;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float hi = __bfloat162float(__float2bfloat16_rn(pr[g]));
-        pc[g] = hi;
-        pc[LO + g] = pr[g] - hi;
+        const uint32_t hb = __float_as_uint(pr[g]) & 0xffff0000u;
+        pc[g] = hb >> 16;
+        pc[LO + g] = __float_as_uint(pr[g] - __uint_as_float(hb)) >> 16;
       }
       uint32_t wp[NP / 2];
 #pragma unroll
-      for (int k = 0; k < NP / 2; ++k) wp[k] = pack_bf16(pc[2 * k], pc[2 * k + 1]);
+      for (int k = 0; k < NP / 2; ++k) wp[k] = pc[2 * k] | (pc[2 * k + 1] << 16);
       wait(&gb[kPEmpty + b], ph ^ 1u, aborted);
       unsigned char* prow = gp + b * PB + (r >> 3) * (PGRP * 128) + (r & 7) * 16;
 #pragma unroll
