@@ -474,9 +474,12 @@ def gpu_arm(args):
                       partition_tokens=args.partition_tokens)
 
     # ---------------- device-resident steps ----------------
+    # The K timed steps record no event between the two kernels, so the
+    # decode's set-up can overlap the append as in a serving loop; the decode
+    # kernel's own duration (for the roofline) is timed afterwards with an
+    # event pair around each decode launch.
     for _ in range(Wm):
         step()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -484,11 +487,7 @@ def gpu_arm(args):
     w0 = time.time()
     t0e.record(stream)
     for k in range(K):
-        ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
-        ev[k][0].record(stream)
-        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws,
-                      partition_tokens=args.partition_tokens)
-        ev[k][1].record(stream)
+        step()
     t1e.record(stream)
     torch.cuda.synchronize(dev)
     w1 = time.time()
@@ -496,6 +495,17 @@ def gpu_arm(args):
     if world > 1:
         dist.barrier()
     total_ms = t0e.elapsed_time(t1e)
+    K2 = min(K, 500)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+    w0b = time.time()
+    for k in range(K2):
+        ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
+        ev[k][0].record(stream)
+        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws,
+                      partition_tokens=args.partition_tokens)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark(w0b, time.time())
     dec_ms = [a.elapsed_time(b) for a, b in ev]
     dev_status = ops.pa_workspace_error(ws)
     if dev_status != 0:

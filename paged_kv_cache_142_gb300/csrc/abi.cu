@@ -652,8 +652,20 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
         !encode_rows_128(&tmq, q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(pl.group)))
       return PA_ERR_CUDA;
     void* args[] = {&p, &tmk, &tmv, &tmq};
-    e = cudaLaunchKernel(plan_kernel(pl), dim3(static_cast<unsigned>(ctas)), dim3(kUmmaThreadsHost),
-                         args, static_cast<size_t>(pl.smem), static_cast<cudaStream_t>(stream));
+    // programmatic serialisation: the kernel's set-up may overlap the tail of
+    // the previous kernel on the stream (the append signals it early); the
+    // kernel waits for that kernel's completion before reading any input
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kUmmaThreadsHost);
+    cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, plan_kernel(pl), args);
   } else {
     void* args[] = {&p};
     e = cudaLaunchKernel(pl.info.fn, dim3(static_cast<unsigned>(ctas)), dim3(pa::kDecodeThreads),

@@ -17,6 +17,7 @@
 // (copy), so every global access is coalesced.  Out-of-range slots / blocks
 // are skipped, never written.
 #include "decode.cuh"
+#include "ptx.cuh"
 
 namespace pa {
 namespace {
@@ -29,6 +30,9 @@ __global__ void __launch_bounds__(256)
                              const int64_t* __restrict__ slots, uint4* __restrict__ k_cache,
                              uint4* __restrict__ v_cache, int64_t cache_layer_chunks,
                              int64_t num_slots, int32_t bs, int32_t hkv, int32_t chunks) {
+  // a decode launched behind this append may begin its set-up now; it waits
+  // for this grid's writes before reading the cache
+  ptx::griddep_launch_dependents();
   const int32_t per_token = hkv * chunks;  // 16-byte chunks of one token's K (all kv heads)
   const int64_t total = static_cast<int64_t>(num_tokens) * per_token;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;

@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     ptx::tmem_alloc(tmem_slot, TMEM_COLS);
     ptx::tc_fence_before();
   }
+  // launched behind the step's append with programmatic serialisation, the
+  // set-up above overlaps it; every input is read after this point
+  ptx::griddep_wait();
   const int n_tail = build_item_order(p, lens, prefix_full, tail_seq, warp_sums,
                                       reinterpret_cast<int*>(small), tid, kUmmaThreads);  // syncs
   ptx::tc_fence_after();
