@@ -310,22 +310,11 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     del kc, vc
     # paged prefill (tensor cores): 16 prompts of 2048 tokens, causal
     S_, n_, Hq_ = 16, 2048, 32
-    nb_seq = n_ // bs
-    NBp = S_ * nb_seq
-    kpp = torch.randn((NBp, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
-    vpp = torch.randn((NBp, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
-    tab = torch.randperm(NBp, generator=g, device=dev).to(torch.int32).reshape(S_, nb_seq).contiguous()
-    qp = torch.randn((S_ * n_, Hq_, D), generator=g, device=dev).to(torch.bfloat16)
-    op = torch.empty_like(qp)
-    cu = torch.arange(0, (S_ + 1) * n_, n_, dtype=torch.int32, device=dev)
-    st0 = torch.zeros(S_, dtype=torch.int32, device=dev)
-    stat = torch.zeros(1, dtype=torch.int32, device=dev)
-    t_pf = _event_time_us(lambda: ops.pa_prefill(op, qp, kpp, vpp, cu, st0, tab, 1.0 / math.sqrt(D), Hkv, n_,
-                                                 status=stat), 10, stream)
-    flops = S_ * 2.0 * D * Hq_ * n_ * (n_ + 1)
+    pf_launch, flops, stat = _prefill_case(ops, dev, g, S_, n_, Hq_, Hkv, D, bs)
+    t_pf = _event_time_us(pf_launch, 10, stream)
     pf_tflops = flops / (t_pf * 1e-6) / 1e12
     pf_ok = int(stat.item()) == 0
-    del kpp, vpp, qp, op
+    del pf_launch
     # shared-prefix decode: the beam-search workload's last step, 64 sequences
     # = one 3000-token prompt + 32 tokens of their own (the prompt's 187 full
     # blocks shared by all), plain decode against one group of 64
@@ -402,6 +391,51 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
                          "note": "host allocator, SHA-256 block keys; K/V prefill skipped for the "
                                  "cached tokens"},
     }
+
+
+def _prefill_case(ops, dev, g, S_, n_=2048, Hq_=32, Hkv=8, D=128, bs=16):
+    """Causal prefill of S_ prompts of n_ tokens through shuffled blocks:
+    returns a no-argument launcher and the causal algorithmic flops."""
+    import torch
+    nb_seq = n_ // bs
+    NBp = S_ * nb_seq
+    kpp = torch.randn((NBp, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    vpp = torch.randn((NBp, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    tab = torch.randperm(NBp, generator=g, device=dev).to(torch.int32).reshape(S_, nb_seq).contiguous()
+    qp = torch.randn((S_ * n_, Hq_, D), generator=g, device=dev).to(torch.bfloat16)
+    op = torch.empty_like(qp)
+    cu = torch.arange(0, (S_ + 1) * n_, n_, dtype=torch.int32, device=dev)
+    st0 = torch.zeros(S_, dtype=torch.int32, device=dev)
+    stat = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch():
+        ops.pa_prefill(op, qp, kpp, vpp, cu, st0, tab, 1.0 / math.sqrt(D), Hkv, n_, status=stat)
+
+    return launch, S_ * 2.0 * D * Hq_ * n_ * (n_ + 1), stat
+
+
+def prefill_profile(args):
+    """Small prefill case for ncu: --warmup + --steps launches of pa_prefill."""
+    import torch
+    dev = torch.device("cuda", 0)
+    from paged_kv_cache_142_gb300 import build as B_
+    B_.build(quiet=True)
+    from paged_kv_cache_142_gb300 import ops
+    g = torch.Generator(device=dev).manual_seed(1)
+    launch, flops, stat = _prefill_case(ops, dev, g, args.profile_prefill)
+    for _ in range(args.warmup):
+        launch()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        launch()
+    b.record()
+    torch.cuda.synchronize()
+    if int(stat.item()) != 0:
+        raise RuntimeError("pa_prefill reported an error")
+    us = a.elapsed_time(b) * 1000.0 / args.steps
+    print(json.dumps({"profile_prefill": True, "prompts": args.profile_prefill, "tokens_per_prompt": 2048,
+                      "us": round(us, 2), "TFLOP/s": round(flops / (us * 1e-6) / 1e12, 1)}), flush=True)
 
 
 # --------------------------------------------------------------------------
@@ -696,10 +730,15 @@ def main():
                     help="split-K partition size passed to pa_decode (0 = automatic)")
     ap.add_argument("--profile", action="store_true",
                     help="device-resident steps only (no e2e leg, no CPU baseline)")
+    ap.add_argument("--profile-prefill", type=int, default=0, metavar="PROMPTS",
+                    help="profiling case: only pa_prefill on PROMPTS causal prompts of 2048 tokens "
+                         "(32 q / 8 kv heads), --warmup + --steps launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile_prefill:
+        prefill_profile(args)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_arm(args)
