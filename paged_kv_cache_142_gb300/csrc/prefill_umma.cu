@@ -17,7 +17,10 @@
 // each eight tcgen05.mma (M = N = 128, K = 16) with fp32 accumulators in
 // tensor memory (S double-buffered, then O).  P enters the second product as
 // bf16 hi = bf16(p) and lo = bf16(p - hi), two passes of eight MMAs, so each
-// probability keeps about 16 bits.
+// probability keeps about 16 bits.  P is written back into tensor memory
+// over the S tile it came from and read from there as the A operand of P.V,
+// so the two S buffers double-buffer P as well: the softmax of tile t + 1
+// runs while P.V of tile t is in flight.
 //
 // One CTA per SM, 288 threads, persistent over (tile of TQ tokens, sequence,
 // kv head) items, later (longer) tiles first:
@@ -31,10 +34,10 @@
 //    cycles), warp 3 zeroing first the V rows past the end inside the last
 //    16-key step of the item's last tile;
 //  * warps 4-7 own tensor-memory lanes 0-127, one query row per thread: per
-//    tile they load the row of S into registers at once (max, then
-//    exponentials from the same registers), mask keys
-//    past the row's position, run the online softmax in fp32 (log2 domain)
-//    and write P hi/lo to shared memory (128-byte swizzle, K-major).  The
+//    tile they read the row of S from tensor memory (max, then the
+//    exponentials), mask keys past the row's position, run the online
+//    softmax in fp32 (log2 domain) and store the row's P hi/lo over its S
+//    (per 16-key MMA step: 8 columns of hi, then 8 of lo, bf16 pairs).  The
 //    running max is the reference of P and O and is raised only when a row's
 //    max grows by more than 2^8 (then the warp rescales its O rows in tensor
 //    memory), so most tiles leave O alone.  At the item's end each thread
@@ -56,17 +59,17 @@ namespace prefill_detail {
 constexpr int kThreads = 288;  // 9 warps
 constexpr int kTileBytes = 32768;
 constexpr int kOffQ = 0;
-constexpr int kOffPhi = 32768;
-constexpr int kOffPlo = 65536;
-constexpr int kOffK = 98304;                 // 2 stages
+constexpr int kOffK = 32768;                 // 2 stages
 constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
 constexpr int kOffBar = kOffV + 2 * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align the base
 constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only past 2^8
 
 // barriers
+// [S buffer]: kSFull (Q.K^T done), kPFull (P stored over S), kSFree (both
+// P.V passes of the tile done: S, P and every earlier O update are free)
 constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
-              kSFull = 10, kSEmpty = 12, kPFull = 14, kPVDone = 15, kOEmpty = 16, kDrain = 17,
+              kSFull = 10, kSFree = 12, kPFull = 14, kOEmpty = 16, kDrain = 17,
               kVZero = 20, kNumBars = 21;  // drains: Q.K^T, P.V hi, P.V lo; then V-tail zeroed
 constexpr uint32_t kColO = 256;  // O from the hi halves of P; the lo halves' O at kColO + 128
 
@@ -189,6 +192,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x 16, K-major) read from tensor
+// memory, lane m holding row m as 8 columns of bf16 pairs; issued by one thread.
+__device__ __forceinline__ void umma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 }  // namespace prefill_detail
 
 template <int G>
@@ -204,8 +217,6 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* qbuf = smem + kOffQ;
-  unsigned char* phi = smem + kOffPhi;
-  unsigned char* plo = smem + kOffPlo;
   unsigned char* kring = smem + kOffK;
   unsigned char* vring = smem + kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -228,10 +239,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       ptx::mbar_init(&bars[kVFull + s], 1);
       ptx::mbar_init(&bars[kVEmpty + s], 2);  // both P.V warps
       ptx::mbar_init(&bars[kSFull + s], 1);
-      ptx::mbar_init(&bars[kSEmpty + s], 4);
+      ptx::mbar_init(&bars[kSFree + s], 2);  // both P.V warps
+      ptx::mbar_init(&bars[kPFull + s], 4);
     }
-    ptx::mbar_init(&bars[kPFull], 4);
-    ptx::mbar_init(&bars[kPVDone], 2);  // both P.V warps
     ptx::mbar_init(&bars[kOEmpty], 4);
     for (int d = 0; d < 3; ++d) ptx::mbar_init(&bars[kDrain + d], 1);
     ptx::mbar_init(&bars[kVZero], 1);
@@ -315,7 +325,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           const int b = static_cast<int>(sc & 1u);
           const int kslot = static_cast<int>(kc & 1u);
           wait(&bars[kKFull + kslot], (kc >> 1) & 1u, aborted);
-          wait(&bars[kSEmpty + b], ((sc >> 1) & 1u) ^ 1u, aborted);
+          wait(&bars[kSFree + b], ((sc >> 1) & 1u) ^ 1u, aborted);
           if (aborted) break;
           ptx::tc_fence_after();
           const unsigned char* kt = kring + kslot * kTileBytes;
@@ -345,10 +355,10 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   } else if (warp == 3 || warp == 8) {
     // ============ P.V issue: warp 3 the hi halves of P, warp 8 the lo ============
     // Each accumulates into its own O (columns kColO / kColO + 128), so the
-    // two chains issue in parallel; the epilogue adds them.
+    // two chains issue in parallel; the epilogue adds them.  P is the A
+    // operand, read from the tile's S buffer in tensor memory.
     constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, 128, 0, 1);
     const bool lo = warp == 8;
-    const unsigned char* pbase = lo ? plo : phi;
     const uint32_t od = tmem + kColO + (lo ? 128u : 0u);
     uint32_t ic = 0, vc = 0, tc = 0, zc = 0;
     for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
@@ -356,10 +366,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       if (!item_at(p, w, G, it)) continue;
       for (int t = 0; t < it.ntiles; ++t, ++vc, ++tc) {
         const int vslot = static_cast<int>(vc & 1u);
+        const int b = static_cast<int>(tc & 1u);
         unsigned char* vt = vring + vslot * kTileBytes;
         if (lane == 0) {
           wait(&bars[kVFull + vslot], (vc >> 1) & 1u, aborted);
-          wait(&bars[kPFull], tc & 1u, aborted);
+          wait(&bars[kPFull + b], (tc >> 1) & 1u, aborted);
           if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);
@@ -387,10 +398,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           ptx::tc_fence_after();
+          const uint32_t pa = tmem + static_cast<uint32_t>(b * 128) + (lo ? 8u : 0u);
           for (int ks = 0; ks < nks; ++ks)
-            ptx::umma_bf16(od, ptx::smem_desc(pbase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, ptx::kLayoutSw128),
-                           ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128), kIdPV, t > 0 || ks > 0);
-          ptx::umma_commit(&bars[kPVDone]);
+            umma_ts_bf16(od, pa + ks * 16, ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128),
+                         kIdPV, t > 0 || ks > 0);
+          ptx::umma_commit(&bars[kSFree + b]);
           ptx::umma_commit(&bars[kVEmpty + vslot]);
         }
         __syncwarp();
@@ -411,12 +423,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     const int g = r / TQ, trow = r - (r / TQ) * TQ;
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, tc = 0;
-    // 16-byte chunk c (keys 8c .. 8c+7) of this row in a 128-byte-swizzled,
-    // K-major [2 halves][128 rows][128 B] tile
-    auto chunk_addr = [&](unsigned char* base, int c) -> unsigned char* {
-      return base + (c >> 3) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
-    };
+    uint32_t sc = 0;
     // max of the first n (<= 32, may be <= 0) raw scores of a 32-column chunk
     auto chunk_max = [](const uint32_t (&v)[32], int n) -> float {
       float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, m2 = -CUDART_INF_F, m3 = -CUDART_INF_F;
@@ -435,12 +442,14 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       }
       return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
     };
-    // p for the chunk's columns (0 past the first n), added to the four
-    // partial sums, and its P hi/lo row pieces.  hi = p with its low 16 bits
-    // cleared (a bf16 value, exact), lo = the exact fp32 remainder cut the
-    // same way: |p - hi - lo| < 2^-16 p, both packed by bit moves
-    auto write_p = [&](const uint32_t (&v)[32], int c, int n, float neg_m, float (&ls)[4]) {
-      uint32_t hi[16], lo[16];
+    // p for the chunk's 32 columns (0 past the first n), added to the four
+    // partial sums, and the chunk's P hi/lo stored over the same 32 columns
+    // of S: for each of its two 16-key MMA steps, 8 columns of hi pairs, then
+    // 8 of lo pairs (the even key in the low half).  hi = p with its low 16
+    // bits cleared (a bf16 value, exact), lo = the exact fp32 remainder cut
+    // the same way: |p - hi - lo| < 2^-16 p, both packed by bit moves
+    auto write_p = [&](const uint32_t (&v)[32], uint32_t dst, int n, float neg_m, float (&ls)[4]) {
+      uint32_t w[32];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         uint32_t hb[2], lb[2];
@@ -452,16 +461,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           hb[e] = __float_as_uint(pr) & 0xffff0000u;
           lb[e] = __float_as_uint(pr - __uint_as_float(hb[e]));
         }
-        hi[j >> 1] = __byte_perm(hb[0], hb[1], 0x7632);  // high halves: element 0 low, 1 high
-        lo[j >> 1] = __byte_perm(lb[0], lb[1], 0x7632);
+        const int step = j >> 4, pair = (j & 15) >> 1;  // MMA step in the chunk, pair in the step
+        w[step * 16 + pair] = __byte_perm(hb[0], hb[1], 0x7632);      // high halves
+        w[step * 16 + 8 + pair] = __byte_perm(lb[0], lb[1], 0x7632);
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        *reinterpret_cast<uint4*>(chunk_addr(phi, c * 4 + q)) =
-            make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-        *reinterpret_cast<uint4*>(chunk_addr(plo, c * 4 + q)) =
-            make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-      }
+      ptx::tmem_st32(dst, w);
     };
     for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
       Item it;
@@ -493,11 +497,6 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           mraw = fmaxf(mraw, chunk_max(vb, nvis - c * 32 - 32));
         }
         const float mt = mraw * sl2;
-        // P and O are free once the previous tile's P.V is done
-        if (t > 0) {
-          wait(&bars[kPVDone], (tc - 1) & 1u, aborted);
-          ptx::tc_fence_after();
-        }
         const float mn = fmaxf(m_ref, mt);
         bool rescale = t > 0 && mn > m_ref + kRescaleLog2;
         float alpha = 1.f;
@@ -508,7 +507,12 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           m_ref = mn;
           l *= alpha;
         }
-        if (__any_sync(0xffffffffu, rescale)) {  // warp-collective rescale of both O in tensor memory
+        if (__any_sync(0xffffffffu, rescale)) {
+          // warp-collective rescale of both O in tensor memory, once P.V of
+          // the previous tile (and so every earlier one) has landed in O
+          const uint32_t pb = (sc - 1u) & 1u;
+          wait(&bars[kSFree + pb], ((sc - 1u) >> 1) & 1u, aborted);
+          ptx::tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
             uint32_t v[32];
@@ -521,7 +525,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           ptx::tmem_wait_st();
         }
         // pass 2: p = 2^(s * scale_log2 - m_ref) (0 for masked keys), row sum,
-        // P hi/lo rows; S is free once its last chunk is loaded
+        // P hi/lo stored over the columns of S just read
         const float neg_m = -m_ref;
         float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
@@ -530,25 +534,19 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           ptx::TmemLd<32>::run(sbase + c * 32, va);
           ptx::TmemLd<32>::run(sbase + c * 32 + 32, vb);
           ptx::tmem_wait_ld();
-          if (c == 2) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars[kSEmpty + b]);
-          }
-          write_p(va, c, nvis - c * 32, neg_m, lsum);
-          write_p(vb, c + 1, nvis - c * 32 - 32, neg_m, lsum);
+          write_p(va, sbase + c * 32, nvis - c * 32, neg_m, lsum);
+          write_p(vb, sbase + c * 32 + 32, nvis - c * 32 - 32, neg_m, lsum);
         }
         l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars[kPFull]);
+        if (lane == 0) ptx::mbar_arrive(&bars[kPFull + b]);
         ++sc;
-        ++tc;
       }
       if (aborted) break;
-      // epilogue: O row / row sum
-      wait(&bars[kPVDone], (tc - 1) & 1u, aborted);
+      // epilogue: O row / row sum, once the item's last P.V has landed
+      wait(&bars[kSFree + ((sc - 1u) & 1u)], ((sc - 1u) >> 1) & 1u, aborted);
       aborted = __any_sync(0xffffffffu, aborted);
       if (aborted) break;
       ptx::tc_fence_after();
