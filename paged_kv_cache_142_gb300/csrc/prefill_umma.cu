@@ -26,7 +26,7 @@
 // kv head) items, later (longer) tiles first:
 //  * warp 0 loads the item's query rows (2-D TMA boxes, one per head and
 //    64-dim half) and its K tiles (one 4-D TMA box per block, as in decode)
-//    into a 2-stage ring; warp 2 loads the V tiles likewise;
+//    into a ring of kRingStages; warp 2 loads the V tiles likewise;
 //  * warp 1 issues Q.K^T of every tile as soon as its K tile has landed and
 //    an S buffer is free (so the softmax of tile t overlaps Q.K^T of t + 1);
 //  * warps 3 and 8 issue P.V of the hi and the lo halves of P into two O
@@ -58,19 +58,23 @@ namespace prefill_detail {
 
 constexpr int kThreads = 288;  // 9 warps
 constexpr int kTileBytes = 32768;
+constexpr int kRingStages = 2;               // K ring and V ring depth
 constexpr int kOffQ = 0;
-constexpr int kOffK = 32768;                 // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;  // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kOffK = 32768;
+constexpr int kOffV = kOffK + kRingStages * kTileBytes;
+constexpr int kOffBar = kOffV + kRingStages * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align the base
 constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only past 2^8
 
 // barriers
 // [S buffer]: kSFull (Q.K^T done), kPFull (P stored over S), kSFree (both
 // P.V passes of the tile done: S, P and every earlier O update are free)
-constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
-              kSFull = 10, kSFree = 12, kPFull = 14, kOEmpty = 16, kDrain = 17,
-              kVZero = 20, kNumBars = 21;  // drains: Q.K^T, P.V hi, P.V lo; then V-tail zeroed
+constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = kKFull + kRingStages,
+              kVFull = kKEmpty + kRingStages, kVEmpty = kVFull + kRingStages, kSFull = kVEmpty + kRingStages,
+              kSFree = kSFull + 2, kPFull = kSFree + 2, kOEmpty = kPFull + 2, kDrain = kOEmpty + 1,
+              kVZero = kDrain + 3, kNumBars = kVZero + 1;  // drains: Q.K^T, P.V hi, P.V lo; then V-tail zeroed
+static_assert(kNumBars * 8 + 8 + 4 <= 256, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kColO = 256;  // O from the hi halves of P; the lo halves' O at kColO + 128
 
 struct Item {
@@ -233,11 +237,13 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   if (tid == 0) {
     ptx::mbar_init(&bars[kQFull], 1);
     ptx::mbar_init(&bars[kQEmpty], 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kRingStages; ++s) {
       ptx::mbar_init(&bars[kKFull + s], 1);
       ptx::mbar_init(&bars[kKEmpty + s], 1);
       ptx::mbar_init(&bars[kVFull + s], 1);
       ptx::mbar_init(&bars[kVEmpty + s], 2);  // both P.V warps
+    }
+    for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bars[kSFull + s], 1);
       ptx::mbar_init(&bars[kSFree + s], 2);  // both P.V warps
       ptx::mbar_init(&bars[kPFull + s], 4);
@@ -285,8 +291,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       }
       const int32_t* trow = p.block_tables + static_cast<int64_t>(it.trow_seq) * p.max_blocks_per_seq;
       for (int t = 0; t < it.ntiles && !aborted; ++t, ++fc) {
-        const int slot = static_cast<int>(fc & 1u);
-        const uint32_t ph = (fc >> 1) & 1u;
+        const int slot = static_cast<int>(fc % kRingStages);
+        const uint32_t ph = (fc / kRingStages) & 1u;
         const int nv = min(128, it.kend - it.k_start - t * 128);
         const int nbox = (nv + box_rows - 1) / box_rows;
         int row = 0;
@@ -323,8 +329,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         wait(&bars[kQFull], ic & 1u, aborted);
         for (int t = 0; t < it.ntiles && !aborted; ++t, ++kc, ++sc) {
           const int b = static_cast<int>(sc & 1u);
-          const int kslot = static_cast<int>(kc & 1u);
-          wait(&bars[kKFull + kslot], (kc >> 1) & 1u, aborted);
+          const int kslot = static_cast<int>(kc % kRingStages);
+          wait(&bars[kKFull + kslot], (kc / kRingStages) & 1u, aborted);
           wait(&bars[kSFree + b], ((sc >> 1) & 1u) ^ 1u, aborted);
           if (aborted) break;
           ptx::tc_fence_after();
@@ -365,11 +371,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       Item it;
       if (!item_at(p, w, G, it)) continue;
       for (int t = 0; t < it.ntiles; ++t, ++vc, ++tc) {
-        const int vslot = static_cast<int>(vc & 1u);
+        const int vslot = static_cast<int>(vc % kRingStages);
         const int b = static_cast<int>(tc & 1u);
         unsigned char* vt = vring + vslot * kTileBytes;
         if (lane == 0) {
-          wait(&bars[kVFull + vslot], (vc >> 1) & 1u, aborted);
+          wait(&bars[kVFull + vslot], (vc / kRingStages) & 1u, aborted);
           wait(&bars[kPFull + b], (tc >> 1) & 1u, aborted);
           if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
         }
@@ -450,20 +456,31 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
     // the same way: |p - hi - lo| < 2^-16 p, both packed by bit moves
     auto write_p = [&](const uint32_t (&v)[32], uint32_t dst, int n, float neg_m, float (&ls)[4]) {
       uint32_t w[32];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        uint32_t hb[2], lb[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float pr = fast_exp2(fmaf(__uint_as_float(v[j + e]), sl2, neg_m));
-          if (n < 32) pr = j + e < n ? pr : 0.f;
-          ls[(j + e) & 3] += pr;
-          hb[e] = __float_as_uint(pr) & 0xffff0000u;
-          lb[e] = __float_as_uint(pr - __uint_as_float(hb[e]));
-        }
+      auto put = [&](int j, float p0, float p1) {
+        const uint32_t h0 = __float_as_uint(p0) & 0xffff0000u, h1 = __float_as_uint(p1) & 0xffff0000u;
         const int step = j >> 4, pair = (j & 15) >> 1;  // MMA step in the chunk, pair in the step
-        w[step * 16 + pair] = __byte_perm(hb[0], hb[1], 0x7632);      // high halves
-        w[step * 16 + 8 + pair] = __byte_perm(lb[0], lb[1], 0x7632);
+        w[step * 16 + pair] = __byte_perm(h0, h1, 0x7632);  // high halves
+        w[step * 16 + 8 + pair] = __byte_perm(__float_as_uint(p0 - __uint_as_float(h0)),
+                                              __float_as_uint(p1 - __uint_as_float(h1)), 0x7632);
+      };
+      if (n >= 32) {  // the common case: every key visible
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(v[j]), sl2, neg_m));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(v[j + 1]), sl2, neg_m));
+          ls[j & 3] += p0;
+          ls[(j + 1) & 3] += p1;
+          put(j, p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = j < n ? fast_exp2(fmaf(__uint_as_float(v[j]), sl2, neg_m)) : 0.f;
+          const float p1 = j + 1 < n ? fast_exp2(fmaf(__uint_as_float(v[j + 1]), sl2, neg_m)) : 0.f;
+          ls[j & 3] += p0;
+          ls[(j + 1) & 3] += p1;
+          put(j, p0, p1);
+        }
       }
       ptx::tmem_st32(dst, w);
     };
