@@ -25,7 +25,8 @@
 // One CTA per SM, 288 threads, persistent over (tile of TQ tokens, sequence,
 // kv head) items, later (longer) tiles first:
 //  * warp 0 loads the item's query rows (2-D TMA boxes, one per head and
-//    64-dim half) and its K tiles (one 4-D TMA box per block, as in decode)
+//    64-dim half; two buffers, so the next item's rows load during this
+//    item) and its K tiles (one 4-D TMA box per block, as in decode)
 //    into a ring of kRingStages; warp 2 loads the V tiles likewise;
 //  * warp 1 issues Q.K^T of every tile as soon as its K tile has landed and
 //    an S buffer is free (so the softmax of tile t overlaps Q.K^T of t + 1);
@@ -59,8 +60,8 @@ namespace prefill_detail {
 constexpr int kThreads = 288;  // 9 warps
 constexpr int kTileBytes = 32768;
 constexpr int kRingStages = 2;               // K ring and V ring depth
-constexpr int kOffQ = 0;
-constexpr int kOffK = 32768;
+constexpr int kOffQ = 0;                     // 2 query buffers (consecutive items)
+constexpr int kOffK = 65536;
 constexpr int kOffV = kOffK + kRingStages * kTileBytes;
 constexpr int kOffBar = kOffV + kRingStages * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align the base
@@ -69,7 +70,7 @@ constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only pa
 // barriers
 // [S buffer]: kSFull (Q.K^T done), kPFull (P stored over S), kSFree (both
 // P.V passes of the tile done: S, P and every earlier O update are free)
-constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = kKFull + kRingStages,
+constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = kKFull + kRingStages,
               kVFull = kKEmpty + kRingStages, kVEmpty = kVFull + kRingStages, kSFull = kVEmpty + kRingStages,
               kSFree = kSFull + 2, kPFull = kSFree + 2, kOEmpty = kPFull + 2, kDrain = kOEmpty + 1,
               kVZero = kDrain + 3, kNumBars = kVZero + 1;  // drains: Q.K^T, P.V hi, P.V lo; then V-tail zeroed
@@ -235,8 +236,10 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
                                   : p.num_seqs * hkv;
 
   if (tid == 0) {
-    ptx::mbar_init(&bars[kQFull], 1);
-    ptx::mbar_init(&bars[kQEmpty], 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bars[kQFull + s], 1);
+      ptx::mbar_init(&bars[kQEmpty + s], 1);
+    }
     for (int s = 0; s < kRingStages; ++s) {
       ptx::mbar_init(&bars[kKFull + s], 1);
       ptx::mbar_init(&bars[kKEmpty + s], 1);
@@ -282,12 +285,13 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       Item it;
       if (!item_at(p, w, G, it)) continue;
       if (!is_v && lane == 0) {
-        wait(&bars[kQEmpty], (ic & 1u) ^ 1u, aborted);
-        ptx::mbar_arrive_expect_tx(&bars[kQFull], 2u * 128u * 128u);
+        const uint32_t qs = ic & 1u;
+        wait(&bars[kQEmpty + qs], ((ic >> 1) & 1u) ^ 1u, aborted);
+        ptx::mbar_arrive_expect_tx(&bars[kQFull + qs], 2u * 128u * 128u);
         for (int g = 0; g < G; ++g)
           for (int h = 0; h < 2; ++h)
-            ptx::tma_load_2d(qbuf + h * 16384 + g * TQ * 128, &tm_q, (it.kvh * G + g) * 128 + h * 64,
-                             it.qb + it.tok0, &bars[kQFull], pol_q);
+            ptx::tma_load_2d(qbuf + qs * 32768 + h * 16384 + g * TQ * 128, &tm_q,
+                             (it.kvh * G + g) * 128 + h * 64, it.qb + it.tok0, &bars[kQFull + qs], pol_q);
       }
       const int32_t* trow = p.block_tables + static_cast<int64_t>(it.trow_seq) * p.max_blocks_per_seq;
       for (int t = 0; t < it.ntiles && !aborted; ++t, ++fc) {
@@ -326,7 +330,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       Item it;
       if (!item_at(p, w, G, it)) continue;
       if (lane == 0) {
-        wait(&bars[kQFull], ic & 1u, aborted);
+        const uint32_t qs = ic & 1u;
+        const unsigned char* qt = qbuf + qs * 32768;
+        wait(&bars[kQFull + qs], (ic >> 1) & 1u, aborted);
         for (int t = 0; t < it.ntiles && !aborted; ++t, ++kc, ++sc) {
           const int b = static_cast<int>(sc & 1u);
           const int kslot = static_cast<int>(kc % kRingStages);
@@ -339,13 +345,13 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const int h = kk >> 2, k4 = kk & 3;
-            ptx::umma_bf16(sd, ptx::smem_desc(qbuf + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
+            ptx::umma_bf16(sd, ptx::smem_desc(qt + h * 16384 + k4 * 32, 16, 1024, ptx::kLayoutSw128),
                            ptx::smem_desc(kt + h * 1024 + k4 * 32, 16, 2048, ptx::kLayoutSw128), kIdQK,
                            kk > 0);
           }
           ptx::umma_commit(&bars[kSFull + b]);
           ptx::umma_commit(&bars[kKEmpty + kslot]);
-          if (t == it.ntiles - 1) ptx::umma_commit(&bars[kQEmpty]);
+          if (t == it.ntiles - 1) ptx::umma_commit(&bars[kQEmpty + qs]);
         }
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
