@@ -116,3 +116,36 @@ def test_chunk_outside_the_table_is_reported_and_skipped(ops):
                                _bf16_f64(c["kv"].bits[1]), c["tables"][:1], c["cu"][:2], c["starts"][:1],
                                0.1, c["Hkv"])
     assert float(np.abs(to_f64(out)[:40] - ref).max()) <= TOL["bf16"]
+
+
+def test_scores_rising_along_the_keys(ops):
+    """Key magnitudes stepped up along the positions so the running max of
+    later rows grows by far more than 2^8 at several points: inside the first
+    tile, in the first and second halves of the second tile, and in later
+    tiles.  Every growth forces the reference max up, rescaling the partial
+    output (and the tile's probabilities already formed) by the factor
+    2^(m_old - m_new)."""
+    G, bs, Hkv, D = 4, 16, 2, 128
+    n = 520
+    rng = np.random.default_rng(31)
+    H = G * Hkv
+    nb = -(-n // bs)
+    NB = nb + 3
+    tables = rng.permutation(NB)[:nb].astype(np.int32)[None, :]
+    step = np.zeros(n)
+    for pos, mag in ((40, 1.0), (150, 2.5), (230, 4.0), (300, 5.5), (450, 7.0)):
+        step[pos:] = mag
+    # key rows of position t: step(t) * ones + noise, queries ~ ones: score ~ 11.3 * step(t)
+    k_tok = step[:, None, None] + 0.1 * rng.standard_normal((n, Hkv, D))
+    v_tok = rng.standard_normal((n, Hkv, D)) * 0.5
+    kv = np.zeros((2, NB, Hkv, bs, D), dtype=np.float32)
+    for t in range(n):
+        kv[0, tables[0, t // bs], :, t % bs] = k_tok[t]
+        kv[1, tables[0, t // bs], :, t % bs] = v_tok[t]
+    q = 1.0 + 0.05 * rng.standard_normal((n, H, D))
+    c = dict(H=H, Hkv=Hkv, D=D, bs=bs, NB=NB, tables=tables, kv=W.Values.from_f32(kv, "bf16"),
+             cu=np.array([0, n], dtype=np.int32), q=W.Values.from_f32(q.astype(np.float32), "bf16"),
+             starts=np.array([0], dtype=np.int32), max_q=n)
+    out, ref, st = _run(ops, c)
+    assert st == 0
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
