@@ -1,5 +1,8 @@
 """Shared-prefix decode (each group's shared blocks read once for all its
-members) against the oracle's decode and against pa_decode."""
+members) against the oracle's decode and against pa_decode.
+
+The oracle's cache is a host copy that the oracle's own reshape_and_cache and
+copy_blocks fill from the same inputs, slots and copy pairs as the device's."""
 import numpy as np
 import pytest
 import torch
@@ -17,8 +20,18 @@ def ops(lib):
     return importlib.import_module("paged_kv_cache_142_gb300.ops")
 
 
-def _bf16_f64(t: torch.Tensor) -> np.ndarray:
-    return t.detach().float().cpu().numpy().astype(np.float64)
+class _Mirror:
+    """The device cache's host twin, written only by the oracle."""
+
+    def __init__(self, shape):
+        self.k = np.zeros(shape, dtype=np.float32)
+        self.v = np.zeros(shape, dtype=np.float32)
+
+    def append(self, key, value, slots):
+        oracle.reshape_and_cache(key.f32, value.f32, self.k, self.v, np.asarray(slots))
+
+    def copy(self, pairs):
+        oracle.copy_blocks(self.k, self.v, np.asarray(pairs))
 
 
 def _common_prefix_blocks(tables, lens, members, bs):
@@ -53,10 +66,12 @@ def test_beam_search_shared_prefix_decode(ops, bs):
     ga = ops.BlockAllocator(wl.num_blocks, bs, wl.free_order)
     kc = torch.zeros((wl.num_blocks, Hkv, bs, D), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
+    mirror = _Mirror(tuple(kc.shape))
     root = ga.seq_create()
     slots = ga.append_tokens(root, wl.prefix_len)
     ops.pa_reshape_and_cache(to_device(wl.prefix_key), to_device(wl.prefix_value),
                              torch.from_numpy(slots).cuda(), kc, vc)
+    mirror.append(wl.prefix_key, wl.prefix_value, slots)
     beams = [ga.fork(root) for _ in range(S)]
     ga.free_seq(root)
     maxb = -(-(wl.prefix_len + wl.steps) // bs)
@@ -72,8 +87,10 @@ def test_beam_search_shared_prefix_decode(ops, bs):
         slots, pairs = ga.append_slots(beams)
         if len(pairs):
             ops.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).cuda())
+            mirror.copy(pairs)
         ops.pa_reshape_and_cache(to_device(wl.step_key[step]), to_device(wl.step_value[step]),
                                  torch.from_numpy(slots).cuda(), kc, vc)
+        mirror.append(wl.step_key[step], wl.step_value[step], slots)
         if step not in (0, wl.steps // 2, wl.steps - 1):
             continue
         tables, lens = ga.export_tables(beams, maxb)
@@ -81,7 +98,7 @@ def test_beam_search_shared_prefix_decode(ops, bs):
         plain = torch.empty((S, H, D), dtype=torch.float32, device="cuda")
         ops.pa_decode(plain, q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
                       wl.scale, Hkv, max_len, ws)
-        ref = oracle.paged_decode(_bf16_f64(q), _bf16_f64(kc), _bf16_f64(vc), tables, lens, wl.scale, Hkv)
+        ref = oracle.paged_decode(wl.step_q[step].f32, mirror.k, mirror.v, tables, lens, wl.scale, Hkv)
         # one group of all sequences (the prompt's full blocks), then the 16 beam groups
         for groups in ([list(range(S))], [list(range(g * wl.beam, (g + 1) * wl.beam)) for g in range(wl.groups)]):
             out, st, prefix = _shared_decode(ops, q, kc, vc, tables, lens, wl.scale, Hkv, groups, bs)
@@ -102,6 +119,7 @@ def test_random_groups(ops, G):
     ga = ops.BlockAllocator(NB, bs, rng.permutation(NB).astype(np.int32))
     kc = torch.zeros((NB, Hkv, bs, D), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
+    mirror = _Mirror(tuple(kc.shape))
     spec = [(5, 480), (1, 0), (3, 32), (40, 160), (1, 0), (2, 1024), (3, 0)]  # (members, prefix tokens)
     seqs, groups = [], []
     for members, P in spec:
@@ -110,6 +128,7 @@ def test_random_groups(ops, G):
             sl = ga.append_tokens(root, P)
             kv = W.Values.from_f32((rng.standard_normal((2, P, Hkv, D)) * 0.5).astype(np.float32), "bf16")
             ops.pa_reshape_and_cache(to_device(kv[0]), to_device(kv[1]), torch.from_numpy(sl).cuda(), kc, vc)
+            mirror.append(kv[0], kv[1], sl)
         g = []
         for m in range(members):
             s = ga.fork(root)
@@ -118,16 +137,18 @@ def test_random_groups(ops, G):
                 sl = ga.append_tokens(s, extra)
                 kv = W.Values.from_f32((rng.standard_normal((2, extra, Hkv, D)) * 0.5).astype(np.float32), "bf16")
                 ops.pa_reshape_and_cache(to_device(kv[0]), to_device(kv[1]), torch.from_numpy(sl).cuda(), kc, vc)
+                mirror.append(kv[0], kv[1], sl)
             g.append(len(seqs))
             seqs.append(s)
         ga.free_seq(root)
         groups.append(g)
     tables, lens = ga.export_tables(seqs, 80)
-    q = to_device(W.Values.from_f32(rng.standard_normal((len(seqs), H, D)).astype(np.float32), "bf16"))
+    qv = W.Values.from_f32(rng.standard_normal((len(seqs), H, D)).astype(np.float32), "bf16")
+    q = to_device(qv)
     scale = float(np.float32(1 / np.sqrt(D)))
     out, st, prefix = _shared_decode(ops, q, kc, vc, tables, lens, scale, Hkv, groups, bs)
     assert st == 0
     # a one-member group may use all its whole blocks as its "prefix"
     assert [pf for pf, (m, _) in zip(prefix, spec) if m > 1] == [P for m, P in spec if m > 1]
-    ref = oracle.paged_decode(_bf16_f64(q), _bf16_f64(kc), _bf16_f64(vc), tables, lens, scale, Hkv)
+    ref = oracle.paged_decode(qv.f32, mirror.k, mirror.v, tables, lens, scale, Hkv)
     assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
