@@ -351,6 +351,43 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     unique_blocks = len(set(tb[:, :int(ln.max()) // bs + 1].ravel().tolist()))
     sp_ok = int(st_sp.item()) == 0
     del ksp, vsp
+    # decode on the other decode configurations: MHA (G = 1) and long-context
+    # split-K (G = 8, block 16 and 32).  Lengths, pool and free list are the
+    # workloads'; the values are drawn on the device (throughput only; parity
+    # is covered by the tests).  Every launch reads > 1 GB, larger than L2.
+    hbm_peak, _ = measured_peaks()
+    other = {}
+    for label, wl_o in (("mha_bf16: 64 seqs, 32 q = 32 kv heads, lens U[128,2048], block 16",
+                         W.mha_bf16(values=False)),
+                        ("long_bf16: 8 seqs, 64 q / 8 kv heads, len 32768, block 16",
+                         W.long_bf16(block_size=16, values=False)),
+                        ("long_bf16: 8 seqs, 64 q / 8 kv heads, len 32768, block 32",
+                         W.long_bf16(block_size=32, values=False))):
+        Bo, Ho, Hko, Do, bso = wl_o.num_seqs, wl_o.num_q_heads, wl_o.num_kv_heads, wl_o.head_dim, wl_o.block_size
+        ao = ops.BlockAllocator(wl_o.num_blocks, bso, wl_o.free_order)
+        so = [ao.seq_create() for _ in range(Bo)]
+        for s_, n_o in zip(so, wl_o.context_lens):
+            ao.append_tokens(s_, int(n_o))
+        tbo, lno = ao.export_tables(so, wl_o.max_blocks_per_seq)
+        ao.close()
+        kco = (torch.randn((wl_o.num_blocks, Hko, bso, Do), generator=g, device=dev, dtype=torch.bfloat16)
+               * wl_o.sigma)
+        vco = (torch.randn((wl_o.num_blocks, Hko, bso, Do), generator=g, device=dev, dtype=torch.bfloat16)
+               * wl_o.sigma)
+        qo = torch.randn((Bo, Ho, Do), generator=g, device=dev, dtype=torch.bfloat16) * wl_o.sigma
+        oo = torch.empty_like(qo)
+        mlo = int(lno.max())
+        wso = ops.make_workspace(Bo, Ho, Hko, Do, bso, "bf16", mlo, device=dev)
+        d_tbo, d_lno = torch.from_numpy(tbo).to(dev), torch.from_numpy(lno).to(dev)
+        t_o = _event_time_us(lambda: ops.pa_decode(oo, qo, kco, vco, d_tbo, d_lno, wl_o.scale, Hko, mlo, wso),
+                             20, stream)
+        ok_o = ops.pa_workspace_error(wso) == 0
+        by_o = int(lno.sum()) * Hko * Do * 2 * 2 + 2 * Bo * Ho * Do * 2
+        pt_o, ctas_o = ops.pa_decode_plan(Bo, Ho, Hko, Do, bso, "bf16", mlo, 0)
+        other[label] = {"us": round(t_o, 2), "bytes": by_o, "GB/s": gbs(by_o, t_o),
+                        "frac_of_measured_hbm": round(by_o / (t_o * 1e-6) / 1e9 / hbm_peak, 4),
+                        "partition_tokens": pt_o, "status_ok": ok_o}
+        del kco, vco, qo, oo, wso
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
@@ -384,6 +421,7 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
                                  "logical_GB/s_pa_decode": gbs(logical, t_plain),
                                  "logical_GB/s_shared_prefix": gbs(logical, t_shared), "status_ok": sp_ok,
                                  "note": "the unique K/V fits in L2: logical bytes are what the tables name"},
+        "decode_other_configs": other,
         "prefix_cache": {"requests": len(reqs), "tokens_per_request": 3032,
                          "cached_tokens_per_hit": int(hits[1]), "hits": int(sum(h > 0 for h in hits)),
                          "blocks_used": int(used), "blocks_without_cache": 64 * 190,

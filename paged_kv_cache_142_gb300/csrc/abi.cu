@@ -90,12 +90,13 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   // cores: of the 128-token tile); at most part/2 partitions per sequence
   const int64_t unit = pl->umma ? 128 : pl->info.tokens_per_stage;
   const int64_t gran = block_size > unit ? block_size : unit;
-  // tensor cores: long partitions (few epilogues and merges), halved while the
-  // (sequence, kv head, partition) items would not give every SM two; CUDA
-  // cores: 256
+  // tensor cores: long partitions (each item costs a block-table load, a
+  // query load and an epilogue; fewer items mean fewer merges), 4096 tokens
+  // for contexts past 4096 and 2048 otherwise, halved while the (sequence, kv
+  // head, partition) items would not give every SM two; CUDA cores: 256
   int64_t def_pt = kDefaultPartTokens;
   if (pl->umma) {
-    def_pt = 2048;
+    def_pt = max_context_len > 4096 ? 4096 : 2048;
     const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
     while (def_pt > 256 && units * ceil_div(max_context_len, def_pt) < 2 * kSmCountHint) def_pt /= 2;
   }

@@ -134,7 +134,7 @@ class DecodeWorkload:
     num_blocks: int
     context_lens: np.ndarray          # int32 [B]
     free_order: np.ndarray            # int32 [NB], a permutation of 0..NB-1
-    q: Values                         # [B, H, D]
+    q: Values                         # [B, H, D] (None when drawn without values)
     key_hist: Values                  # [sum(len), Hkv, D]
     value_hist: Values                # [sum(len), Hkv, D]
     scale: float
@@ -166,14 +166,19 @@ def _pool_for(lens: np.ndarray, bs: int, factor: float) -> int:
     return int(math.ceil(factor * need)) if factor != 1.0 else need
 
 
-def _make(name, dtype, lens, H, Hkv, D, bs, NB, sigma, seed, rng, extra=None) -> DecodeWorkload:
+def _make(name, dtype, lens, H, Hkv, D, bs, NB, sigma, seed, rng, extra=None,
+          values: bool = True) -> DecodeWorkload:
+    """values=False skips drawing Q/K/V (q, key_hist and value_hist are None);
+    lengths and the free-list order are drawn first, so they are the same."""
     lens = np.asarray(lens, dtype=np.int32)
     B = len(lens)
     free_order = rng.permutation(NB).astype(np.int32)
     T = int(lens.sum())
-    q = Values.from_f32(_normal(rng, (B, H, D), sigma), dtype)
-    k = Values.from_f32(_normal(rng, (T, Hkv, D), sigma), dtype)
-    v = Values.from_f32(_normal(rng, (T, Hkv, D), sigma), dtype)
+    q = k = v = None
+    if values:
+        q = Values.from_f32(_normal(rng, (B, H, D), sigma), dtype)
+        k = Values.from_f32(_normal(rng, (T, Hkv, D), sigma), dtype)
+        v = Values.from_f32(_normal(rng, (T, Hkv, D), sigma), dtype)
     return DecodeWorkload(
         name=name, dtype=dtype, num_seqs=B, num_q_heads=H, num_kv_heads=Hkv,
         head_dim=D, block_size=bs, num_blocks=NB, context_lens=lens,
@@ -188,11 +193,11 @@ def tiny_fp32(seed: int = SEEDS["tiny_fp32"]) -> DecodeWorkload:
 
 
 def mha_bf16(seed: int = SEEDS["mha_bf16"], num_seqs: int = 64,
-             len_range=(128, 2048)) -> DecodeWorkload:
+             len_range=(128, 2048), values: bool = True) -> DecodeWorkload:
     rng = np.random.Generator(np.random.PCG64(seed))
     lens = rng.integers(len_range[0], len_range[1], size=num_seqs, endpoint=True)
     NB = _pool_for(lens, 16, 1.2)
-    return _make("mha_bf16", DTYPE_BF16, lens, 32, 32, 128, 16, NB, 1.0, seed, rng)
+    return _make("mha_bf16", DTYPE_BF16, lens, 32, 32, 128, 16, NB, 1.0, seed, rng, values=values)
 
 
 def gqa_lens(rng: np.random.Generator, num_seqs: int, median: float = 800.0,
@@ -211,11 +216,11 @@ def gqa_bf16(seed: int = SEEDS["gqa_bf16"], num_seqs: int = 256,
 
 
 def long_bf16(seed: int = SEEDS["long_bf16"], block_size: int = 16, num_seqs: int = 8,
-              context_len: int = 32768) -> DecodeWorkload:
+              context_len: int = 32768, values: bool = True) -> DecodeWorkload:
     rng = np.random.Generator(np.random.PCG64(seed + block_size))
     lens = np.full(num_seqs, context_len, dtype=np.int32)
     NB = _pool_for(lens, block_size, 1.0)
-    return _make("long_bf16", DTYPE_BF16, lens, 64, 8, 128, block_size, NB, 1.0, seed, rng)
+    return _make("long_bf16", DTYPE_BF16, lens, 64, 8, 128, block_size, NB, 1.0, seed, rng, values=values)
 
 
 def custom(name: str, dtype: str, lens, num_q_heads: int, num_kv_heads: int, head_dim: int,

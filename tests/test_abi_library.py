@@ -42,19 +42,22 @@ def test_workspace_size_plan_is_host_only(lib):
     small = lib.pa_decode_workspace_size(8, 64, 8, 128, 16, 1, 256, 0)
     big = lib.pa_decode_workspace_size(8, 64, 8, 128, 16, 1, 32768, 0)
     assert 0 < small < big
-    # 8 seqs * 8 kv heads * 16 partitions of 2048 tokens * 8 heads * (128 + 2)
+    # 8 seqs * 8 kv heads * 8 partitions of 4096 tokens * 8 heads * (128 + 2)
     # floats, plus header and counters
-    assert big >= 8 * 8 * 16 * 8 * 130 * 4
+    assert big >= 8 * 8 * 8 * 8 * 130 * 4
     # unsupported group size -> 0
     assert lib.pa_decode_workspace_size(1, 48, 2, 128, 16, 1, 100, 0) == 0
     pt = C.c_int32(0)
-    # bf16, head_dim 128: tensor-core kernel, 2048-token partitions when the
-    # (sequence, kv head, partition) items cover every SM twice ...
+    # bf16, head_dim 128: tensor-core kernel, 4096-token partitions past 4096
+    # tokens of context and 2048 up to it, when the (sequence, kv head,
+    # partition) items cover every SM twice ...
     st = lib.pa_decode_plan(8, 64, 8, 128, 16, 1, 32768, 0, C.byref(pt), None)
-    assert st == 0 and pt.value == 2048
+    assert st == 0 and pt.value == 4096
     st = lib.pa_decode_plan(256, 64, 8, 128, 16, 1, 4096, 0, C.byref(pt), None)
     assert st == 0 and pt.value == 2048
     # ... halved down to 256 tokens while they do not
+    st = lib.pa_decode_plan(2, 64, 8, 128, 16, 1, 32768, 0, C.byref(pt), None)
+    assert st == 0 and pt.value == 1024
     st = lib.pa_decode_plan(8, 64, 8, 128, 16, 1, 4096, 0, C.byref(pt), None)
     assert st == 0 and pt.value == 512
     st = lib.pa_decode_plan(1, 64, 8, 128, 16, 1, 4096, 0, C.byref(pt), None)
