@@ -149,3 +149,48 @@ def test_scores_rising_along_the_keys(ops):
     out, ref, st = _run(ops, c)
     assert st == 0
     assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
+
+
+def test_empty_chunks_among_others_and_no_tokens(ops):
+    """Sequences whose chunk is empty (one with K/V history, one without)
+    between non-empty ones, and a call with no tokens at all."""
+    c = _case(4, 16, [(0, 50), (30, 0), (0, 0), (10, 90)], seed=13)
+    out, ref, st = _run(ops, c)
+    assert st == 0
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
+    empty = dict(c)
+    empty["q"] = W.Values.from_f32(np.zeros((0, c["H"], c["D"]), dtype=np.float32), "bf16")
+    empty["cu"] = np.zeros(5, dtype=np.int32)
+    empty["max_q"] = 0
+    out0, ref0, st = _run(ops, empty)
+    assert st == 0 and out0.shape == (0, c["H"], c["D"]) and ref0.shape == (0, c["H"], c["D"])
+
+
+def test_bench_size_sampled_rows(ops):
+    """The bench's prefill launch (16 causal prompts of 2048 tokens, 32 q /
+    8 kv heads, block 16, shuffled blocks): sampled rows against the oracle's
+    attention over each row's visible keys, gathered through the table."""
+    n, S = 2048, 16
+    c = _case(4, 16, [(0, n)] * S, seed=17, Hkv=8)
+    kc = to_device(c["kv"][0]).contiguous()
+    vc = to_device(c["kv"][1]).contiguous()
+    q = to_device(c["q"]).contiguous()
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = float(np.float32(1.0 / np.sqrt(c["D"])))
+    ops.pa_prefill(out, q, kc, vc, torch.from_numpy(c["cu"]).cuda(), torch.from_numpy(c["starts"]).cuda(),
+                   torch.from_numpy(c["tables"]).cuda(), scale, c["Hkv"], n, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.cpu().numpy()
+    assert not np.isnan(got).any()
+    kf = _bf16_f64(c["kv"].bits[0])
+    vf = _bf16_f64(c["kv"].bits[1])
+    rng = np.random.default_rng(18)
+    rows = np.concatenate([[0, n - 1, n, S * n - 1], rng.integers(0, S * n, size=60)])
+    for tok in rows:
+        i, pos = int(tok) // n, int(tok) % n
+        K = oracle.gather_sequence(kf, c["tables"][i], pos + 1)
+        V = oracle.gather_sequence(vf, c["tables"][i], pos + 1)
+        ref = oracle.contiguous_attention(_bf16_f64(c["q"].bits[tok]), K, V, scale)
+        assert float(np.abs(got[tok].astype(np.float64) - ref).max()) <= TOL["bf16"], (i, pos)
