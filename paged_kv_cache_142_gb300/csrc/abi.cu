@@ -52,6 +52,8 @@ pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_
 // Tensor-core kernel layout constants (must match decode_umma.cuh).
 constexpr int kUmmaThreadsHost = 448;
 constexpr int kUmmaTileBytesHost = 32768;
+// per compute group scratch of the tensor-core decode (with an item's totals for G >= 8)
+constexpr int umma_small_bytes_host(int G) { return G >= 8 ? 1280 : 1024; }
 constexpr int kPrefillThreads = 288;  // must match the prefill kernel
 
 struct Plan {
@@ -112,7 +114,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     // lengths | prefix | align slack
     const int64_t pbytes = G <= 8 ? 4096 : 8192;
     const int64_t tbl_stride = round_up(pt / block_size + 1, 4);
-    const int64_t fixed = 2 * 4096 + 2 * 2 * pbytes + 2 * 1024 + 256 + 1024 + 4 * tbl_stride * 4 +
+    const int64_t fixed = 2 * 4096 + 2 * 2 * pbytes + 2 * umma_small_bytes_host(G) + 256 + 1024 + 4 * tbl_stride * 4 +
                           round_up(static_cast<int64_t>(num_seqs) * 4, 16) +
                           2 * round_up((static_cast<int64_t>(num_seqs) + 4) / 4 * 4 * 4, 16) + 1024;
     int sk = 3, sv = 3;
@@ -131,7 +133,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
       pl->off_p = static_cast<int>(off);
       off += 2 * 2 * pbytes;
       pl->off_small = static_cast<int>(off);
-      off += 2 * 1024 + 256;  // per-group scratch, then the two item queues
+      off += 2 * umma_small_bytes_host(G) + 256;  // per-group scratch, then the two item queues
       pl->off_bar = static_cast<int>(off);
       off += 1024;
       pl->off_tbl = static_cast<int>(off);  // [K/V stream][group]

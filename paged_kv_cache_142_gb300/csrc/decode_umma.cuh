@@ -71,7 +71,8 @@ constexpr int kUmmaTile = 128;           // tokens per tile (MMA M)
 constexpr int kUmmaTileBytes = 32768;    // one K or V tile: 16 row groups x 2 halves x 8 rows x 128 B
 constexpr int kUmmaMaxStages = 8;
 constexpr int kUmmaQBytes = 4096;        // query tile: 2 halves x 16 rows x 128 B (one per group)
-constexpr int kUmmaSmallBytes = 1024;    // per group: reductions and rescale factors
+// per group: reductions and rescale factors (G <= 4), plus an item's totals (G >= 8)
+__host__ __device__ constexpr int umma_small_bytes(int G) { return G >= 8 ? 1280 : 1024; }
 constexpr int kUmmaGroupBars = 16;
 constexpr int kUmmaQueue = 8;            // per-group item queue depth
 constexpr int kUmmaQueueReaders = 9;     // V stream, 2 Q.K and 2 P.V warps, a group's 4 compute warps
@@ -391,7 +392,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   int32_t* lens = reinterpret_cast<int32_t*>(smem + p.off_lens);
   int32_t* prefix_full = reinterpret_cast<int32_t*>(smem + p.off_prefix);
   int32_t* tail_seq = prefix_full + ((p.num_seqs + 4) & ~3);
-  volatile int* queue = reinterpret_cast<volatile int*>(small + 2 * kUmmaSmallBytes);  // [group][kUmmaQueue]
+  constexpr int kSmall = umma_small_bytes(G);
+  volatile int* queue = reinterpret_cast<volatile int*>(small + 2 * kSmall);  // [group][kUmmaQueue]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -692,19 +694,29 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const float sl2 = p.scale_log2;
     uint64_t* gb = bars + kGroup0 + cg * kUmmaGroupBars;
     unsigned char* gp = pbuf + cg * 2 * PB;
-    float* red_m = reinterpret_cast<float*>(small + cg * kUmmaSmallBytes);  // [2][4][16]
-    float* red_l = red_m + 2 * 4 * 16;                                      // [4][16]
-    float* alpha_s = red_l + 4 * 16;                                        // [2][16]
+    // An item's totals (final max, row sums) are needed by its epilogue,
+    // which runs after the next tile's softmax.  G <= 4 keeps them in
+    // registers, one copy per tile parity; G >= 8 is short of registers
+    // (128 per thread at 448 threads) and keeps them in shared memory.
+    constexpr bool kTotalsInSmem = G >= 8;
+    constexpr int NF = kTotalsInSmem ? 1 : G;
+    float* red_m = reinterpret_cast<float*>(small + cg * kSmall);  // [2][4][16]
+    float* alpha_s = red_m + 2 * 4 * 16;  // [2][16]
+    float* red_l = alpha_s + 2 * 16;      // registers: [4][16]; shared: [2][4][16] by tile parity
+    float* red_mf = red_l + 2 * 4 * 16;   // shared: [2][16] an item's final max by tile parity
     volatile int* merge_flag = flags + 1 + cg;
     volatile int* gabort = flags + 3 + cg;
 
     float m_run[G], l_thr[G], o_acc[G];
-    float m_fin0[G], l_fin0[G], m_fin1[G], l_fin1[G];
+    float m_fin0[NF], l_fin0[NF], m_fin1[NF], l_fin1[NF];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m_run[g] = -CUDART_INF_F;
       l_thr[g] = 0.f;
       o_acc[g] = 0.f;
+    }
+#pragma unroll
+    for (int g = 0; g < NF; ++g) {
       m_fin0[g] = m_fin1[g] = -CUDART_INF_F;
       l_fin0[g] = l_fin1[g] = 0.f;
     }
@@ -766,15 +778,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
         for (int g = 0; g < G; ++g) alpha_s[b * 16 + g] = al[g];
       }
-      if (last) {
+      if constexpr (!kTotalsInSmem) {
+        if (last) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          if (b) {
-            m_fin1[g] = m_run[g];
-            l_fin1[g] = l_thr[g];
-          } else {
-            m_fin0[g] = m_run[g];
-            l_fin0[g] = l_thr[g];
+          for (int g = 0; g < NF; ++g) {
+            if (b) {
+              m_fin1[g] = m_run[g];
+              l_fin1[g] = l_thr[g];
+            } else {
+              m_fin0[g] = m_run[g];
+              l_fin0[g] = l_thr[g];
+            }
           }
         }
       }
@@ -803,27 +817,62 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&gb[kPFull + b]);
+      if constexpr (kTotalsInSmem) {
+        if (last) {
+          // row sums reduced per warp and the final max (the same in every
+          // thread), taken after P is handed over.  Slot b is next written
+          // two tiles on, past that tile's group barrier, which every warp
+          // reaches only after this item's epilogue.
+          float lw[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) lw[g] = l_thr[g];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int g = 0; g < G; ++g) lw[g] += __shfl_xor_sync(0xffffffffu, lw[g], off);
+          if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) red_l[(b * 4 + cw) * 16 + g] = lw[g];
+          }
+          if (ctid == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) red_mf[b * 16 + g] = m_run[g];
+          }
+        }
+      }
     };
 
     auto epilogue = [&](const Rec& t) {
-      float mf[G], lf[G];
+      float mf[G], L[G];
+      if constexpr (kTotalsInSmem) {
+        // every warp's totals of this item, written in its last tile's softmax
+        const int pb = static_cast<int>(t.ug & 1u);
+        ptx::bar_sync(bar_id, 128);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        mf[g] = (t.ug & 1u) ? m_fin1[g] : m_fin0[g];
-        lf[g] = (t.ug & 1u) ? l_fin1[g] : l_fin0[g];
+        for (int g = 0; g < G; ++g) {
+          mf[g] = red_mf[pb * 16 + g];
+          L[g] = red_l[(pb * 4) * 16 + g] + red_l[(pb * 4 + 1) * 16 + g] + red_l[(pb * 4 + 2) * 16 + g] +
+                 red_l[(pb * 4 + 3) * 16 + g];
+        }
+      } else {
+        float lf[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          mf[g] = (t.ug & 1u) ? m_fin1[g] : m_fin0[g];
+          lf[g] = (t.ug & 1u) ? l_fin1[g] : l_fin0[g];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) lf[g] += __shfl_xor_sync(0xffffffffu, lf[g], off);
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) red_l[cw * 16 + g] = lf[g];
+        }
+        ptx::bar_sync(bar_id, 128);
+#pragma unroll
+        for (int g = 0; g < G; ++g) L[g] = red_l[g] + red_l[16 + g] + red_l[32 + g] + red_l[48 + g];
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g) lf[g] += __shfl_xor_sync(0xffffffffu, lf[g], off);
-      if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) red_l[cw * 16 + g] = lf[g];
-      }
-      ptx::bar_sync(bar_id, 128);
-      float L[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) L[g] = red_l[g] + red_l[16 + g] + red_l[32 + g] + red_l[48 + g];
       const int64_t obase = (static_cast<int64_t>(t.it.seq) * p.num_q_heads + t.it.kvh * G) * HD + r;
       if (t.it.nparts == 1) {
 #pragma unroll
