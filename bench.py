@@ -639,6 +639,8 @@ def gpu_arm(args):
         x["q"].copy_(torch.from_numpy(np.ascontiguousarray(wl.q.bits)).view(torch.bfloat16))
         x["k"].copy_(new_k.cpu())
         x["v"].copy_(new_v.cpu())
+    b_np = [{k_: x[k_].numpy() for k_ in ("slots", "tables", "lens")} for x in hb]
+    seqs_np = np.asarray(seqs2, dtype=np.int32)
     h_out = [torch.empty((B, H, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     d_out = [torch.empty_like(out) for _ in range(2)]
     h_pairs = torch.empty((B, 2), dtype=torch.int64, pin_memory=True)
@@ -668,16 +670,14 @@ def gpu_arm(args):
     def e2e_step():
         j = counter[0] % 2
         counter[0] += 1
-        b = hb[j]
         if used[j]:
             w0_ = time.perf_counter()
             ev_down[j].synchronize()                   # set j's last step is complete
             waited[0] += time.perf_counter() - w0_
-        slots, pairs = alloc2.append_slots(seqs2)      # host allocator: reserve the slots
-        tb, ln = alloc2.export_tables(seqs2, maxb)
-        b["slots"].numpy()[:] = slots
-        b["tables"].numpy()[:] = tb
-        b["lens"].numpy()[:] = ln
+        # host allocator: reserve the slots and export the tables, straight
+        # into the pinned staging area
+        _, pairs = alloc2.append_slots(seqs_np, out=b_np[j]["slots"])
+        _, ln = alloc2.export_tables(seqs_np, maxb, out=(b_np[j]["tables"], b_np[j]["lens"]))
         with torch.cuda.stream(up):
             d_stage[j].copy_(h_stage[j], non_blocking=True)   # all of the step's inputs
             ev_up[j].record(up)

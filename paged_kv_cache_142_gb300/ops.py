@@ -345,11 +345,17 @@ class BlockAllocator:
                 "pa_alloc_append_slot")
         return slot.value, a.value, b.value
 
-    def append_slots(self, seqs):
-        """One append per sequence; returns (slots int64 [n], cow pairs int64 [k, 2])."""
+    def append_slots(self, seqs, out=None):
+        """One append per sequence; returns (slots int64 [n], cow pairs int64
+        [k, 2]); ``out`` = a contiguous int64 array [n] to write the slots into."""
         seqs = np.ascontiguousarray(seqs, dtype=np.int32)
         n = len(seqs)
-        slots = np.empty(n, dtype=np.int64)
+        if out is not None:
+            _need(isinstance(out, np.ndarray) and out.dtype == np.int64 and out.shape == (n,)
+                  and out.flags.c_contiguous, "out must be a contiguous int64 array [n]")
+            slots = out
+        else:
+            slots = np.empty(n, dtype=np.int64)
         pairs = np.empty((max(n, 1), 2), dtype=np.int64)
         ncow = C.c_int32(0)
         done = C.c_int32(0)
@@ -378,12 +384,21 @@ class BlockAllocator:
         L.check(_LIB.pa_alloc_block_table(self._h, seq, _p32(buf), cap, C.byref(n)), "pa_alloc_block_table")
         return buf[:n.value].tolist()
 
-    def export_tables(self, seqs, max_blocks: int, pad_value: int = 0):
-        """(tables int32 [n, max_blocks], lens int32 [n]) for a batch."""
+    def export_tables(self, seqs, max_blocks: int, pad_value: int = 0, out=None):
+        """(tables int32 [n, max_blocks], lens int32 [n]) for a batch; ``out``
+        = (tables, lens) contiguous int32 arrays of those shapes to write into
+        (e.g. views of a pinned staging buffer)."""
         seqs = np.ascontiguousarray(seqs, dtype=np.int32)
         n = len(seqs)
-        tables = np.empty((max(n, 1), max_blocks), dtype=np.int32)
-        lens = np.empty(max(n, 1), dtype=np.int32)
+        if out is not None:
+            tables, lens = out
+            _need(isinstance(tables, np.ndarray) and tables.dtype == np.int32 and tables.shape == (n, max_blocks)
+                  and tables.flags.c_contiguous and isinstance(lens, np.ndarray) and lens.dtype == np.int32
+                  and lens.shape == (n,) and lens.flags.c_contiguous and n > 0,
+                  "out must be contiguous int32 arrays [n, max_blocks] and [n]")
+        else:
+            tables = np.empty((max(n, 1), max_blocks), dtype=np.int32)
+            lens = np.empty(max(n, 1), dtype=np.int32)
         L.check(_LIB.pa_alloc_export_tables(self._h, _p32(seqs), n, _p32(tables), max_blocks,
                                             _p32(lens), pad_value), "pa_alloc_export_tables")
         return tables[:n], lens[:n]

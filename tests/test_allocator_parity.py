@@ -118,3 +118,32 @@ def test_errors(ops):
     c = a.fork(s)
     with pytest.raises(ops.PAError):
         a.append_tokens(c, 1)  # would need a copy: not a bulk append
+
+
+def test_outputs_written_into_caller_arrays(ops):
+    """append_slots / export_tables with caller-provided arrays (e.g. views of
+    a pinned staging buffer) write exactly what they would return."""
+    wl = W.tiny_fp32()
+    a = ops.BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
+    b = ops.BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
+    seqs = [a.seq_create() for _ in range(wl.num_seqs)]
+    assert [b.seq_create() for _ in range(wl.num_seqs)] == seqs
+    for s, n in zip(seqs, wl.context_lens):
+        a.append_tokens(s, int(n))
+        b.append_tokens(s, int(n))
+    stage = np.zeros(64, dtype=np.int64)
+    for _ in range(20):
+        want_slots, want_pairs = a.append_slots(seqs)
+        got_slots, got_pairs = b.append_slots(seqs, out=stage[8:8 + len(seqs)])
+        assert np.array_equal(stage[8:8 + len(seqs)], want_slots) and np.array_equal(got_slots, want_slots)
+        assert np.array_equal(got_pairs, want_pairs)
+    mb = wl.max_blocks_per_seq + 2
+    want_t, want_l = a.export_tables(seqs, mb)
+    buf = np.full(len(seqs) * mb + len(seqs), -7, dtype=np.int32)
+    t_view, l_view = buf[:len(seqs) * mb].reshape(len(seqs), mb), buf[len(seqs) * mb:]
+    b.export_tables(seqs, mb, out=(t_view, l_view))
+    assert np.array_equal(t_view, want_t) and np.array_equal(l_view, want_l)
+    with pytest.raises(ValueError):
+        b.export_tables(seqs, mb, out=(t_view[:, :-1], l_view))
+    with pytest.raises(ValueError):
+        b.append_slots(seqs, out=np.zeros(len(seqs), dtype=np.int32))
