@@ -531,17 +531,13 @@ pa_status pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, 
   p.num_parts = static_cast<int32_t>(parts);
   p.part_ml = static_cast<float*>(workspace);
   p.part_o = p.part_ml + (parts + 1) * rows * 2;
-  // 1: the groups' prefixes, every member's queries against each prefix block once
-  p.mode = 1;
-  st = launch_prefill(p, G, parts * num_groups * num_kv_heads * tiles, q, k_cache, v_cache,
-                      cache_rows, stream);
+  // one launch: the groups' prefixes (every member's queries against each
+  // prefix block once), then every member's own tokens past its group's prefix
+  p.mode = 3;
+  st = launch_prefill(p, G, parts * num_groups * num_kv_heads * tiles + static_cast<int64_t>(num_seqs) * num_kv_heads,
+                      q, k_cache, v_cache, cache_rows, stream);
   if (st != PA_OK) return st;
-  // 2: every member's own tokens past its group's prefix
-  p.mode = 2;
-  st = launch_prefill(p, G, static_cast<int64_t>(num_seqs) * num_kv_heads, q, k_cache, v_cache,
-                      cache_rows, stream);
-  if (st != PA_OK) return st;
-  // 3: log-sum-exp merge into out
+  // then the log-sum-exp merge into out
   cudaError_t e = pa::launch_cascade_merge(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -88,7 +88,7 @@ struct PrefillParams {
   float scale_log2;
   int32_t* status;         // device error word (may be null)
   // shared-prefix decode (mode 1: the groups' prefixes, mode 2: the members'
-  // own tokens past them); mode 0 is causal prefill
+  // own tokens past them, mode 3: both in one launch); mode 0 is causal prefill
   int32_t mode;
   const int32_t* group_start;   // [num_groups + 1] member ranges of the batch
   const int32_t* prefix_len;    // [num_groups] shared tokens (whole blocks)

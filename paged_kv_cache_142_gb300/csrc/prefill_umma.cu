@@ -101,12 +101,22 @@ __device__ __forceinline__ void bad_input(const PrefillParams& p) {
 // later tiles first, causal keys [0, position].  Mode 1 (shared prefix):
 // (prefix partition, tile of TQ members, group, kv head) over the group's
 // prefix keys, read through its first member's table.  Mode 2 (own tokens):
-// (member, kv head) over keys [prefix, len) of the member's table.
+// (member, kv head) over keys [prefix, len) of the member's table.  Mode 3:
+// every mode-1 item, then every mode-2 item, in one launch.
+__device__ __forceinline__ int prefix_items(const PrefillParams& p) {
+  return p.num_parts * p.num_groups * p.num_kv_heads * p.tiles_per_seq;
+}
 __device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, Item& it) {
   const int hkv = p.num_kv_heads;
   const int TQ = 128 / G;
   const int64_t table_tokens = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
-  if (p.mode == 0) {
+  int mode = p.mode;
+  if (mode == 3) {
+    const int n1 = prefix_items(p);
+    mode = w < n1 ? 1 : 2;
+    if (mode == 2) w -= n1;
+  }
+  if (mode == 0) {
     const int per_tile = p.num_seqs * hkv;
     const int tile = p.tiles_per_seq - 1 - w / per_tile;
     const int rem = w - (w / per_tile) * per_tile;
@@ -128,7 +138,7 @@ __device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, It
     it.trow_seq = it.seq;
     it.causal = 1;
     it.part = 0;
-  } else if (p.mode == 1) {
+  } else if (mode == 1) {
     const int per_part = p.num_groups * hkv * p.tiles_per_seq;
     it.part = w / per_part;
     const int rem = w - it.part * per_part;
@@ -232,8 +242,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   const int hkv = p.num_kv_heads, bs = p.block_size;
   const int bs_log = __ffs(bs) - 1;
   const int items = p.mode == 0   ? p.num_seqs * hkv * p.tiles_per_seq
-                    : p.mode == 1 ? p.num_parts * p.num_groups * hkv * p.tiles_per_seq
-                                  : p.num_seqs * hkv;
+                    : p.mode == 1 ? prefix_items(p)
+                    : p.mode == 2 ? p.num_seqs * hkv
+                                  : prefix_items(p) + p.num_seqs * hkv;
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
