@@ -634,6 +634,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   }
 
   // ============================ teardown ============================
+  // a merge launched behind this kernel with programmatic serialisation may
+  // start; it waits for this grid's completion before reading its results
+  ptx::griddep_launch_dependents();
   if (aborted) flags[0] = 1;
   ptx::tc_fence_before();
   __syncthreads();
@@ -648,6 +651,7 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const __grid_constan
   const int rows = p.num_seqs * p.num_q_heads;
   const int row = blockIdx.x;  // member * H + head
   if (row >= rows) return;
+  ptx::griddep_wait();  // launched behind the passes: their partial results are complete past here
   const int i = row / p.num_q_heads;
   const int d = threadIdx.x;
   const int grp = prefill_detail::group_of(p, i);
@@ -681,8 +685,18 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const __grid_constan
 cudaError_t launch_cascade_merge(const PrefillParams& p, cudaStream_t stream) {
   const int rows = p.num_seqs * p.num_q_heads;
   if (rows == 0) return cudaSuccess;
-  cascade_merge_kernel<<<rows, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic serialisation: the launch overlaps the passes' tail
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cascade_merge_kernel, p);
 }
 
 const void* prefill_umma_fn(int group) {
