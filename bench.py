@@ -284,6 +284,28 @@ def _event_time_us(fn, iters: int, stream) -> float:
     return a.elapsed_time(b) * 1000.0 / iters
 
 
+def _graph_time_us(fn, n: int = 20, reps: int = 10) -> float:
+    """Device time per call of fn, replayed from a CUDA graph of n calls (no
+    host dispatch between the kernels)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(n):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1000.0 / (n * reps)
+
+
 def measure_extras(ops, dev, seed: int = 1420) -> dict:
     """Multi-layer append and copy-on-write copy of a decode step, one launch
     for all layers, against one launch per layer (algorithmic bytes: read +
@@ -301,10 +323,12 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     pairs = torch.stack([perm[:pairs_n], perm[pairs_n:2 * pairs_n]], dim=1).to(torch.int64).contiguous()
     append_b = Lyr * T * Hkv * D * 2 * 2 * 2
     copy_b = Lyr * pairs_n * 2 * Hkv * bs * D * 2 * 2
-    t_app = _event_time_us(lambda: ops.pa_reshape_and_cache_layers(key, val, slots, kc, vc), 50, stream)
+    t_app = _graph_time_us(lambda: ops.pa_reshape_and_cache_layers(key, val, slots, kc, vc))
+    t_app_e = _event_time_us(lambda: ops.pa_reshape_and_cache_layers(key, val, slots, kc, vc), 50, stream)
     t_app1 = _event_time_us(lambda: [ops.pa_reshape_and_cache(key[i], val[i], slots, kc[i], vc[i])
                                      for i in range(Lyr)], 20, stream)
-    t_cp = _event_time_us(lambda: ops.pa_copy_blocks_layers(kc, vc, pairs), 50, stream)
+    t_cp = _graph_time_us(lambda: ops.pa_copy_blocks_layers(kc, vc, pairs))
+    t_cp_e = _event_time_us(lambda: ops.pa_copy_blocks_layers(kc, vc, pairs), 50, stream)
     t_cp1 = _event_time_us(lambda: [ops.pa_copy_blocks(kc[i], vc[i], pairs) for i in range(Lyr)], 20, stream)
     gbs = lambda b, us: round(b / (us * 1e-6) / 1e9, 1)
     del kc, vc
@@ -344,9 +368,12 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
                                       shared, status=st_sp)
     t_plain = _event_time_us(lambda: ops.pa_decode(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D), Hkv, mlen,
                                                    wsd), 50, stream)
-    t_shared = _event_time_us(lambda: ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D),
+    t_shared = _graph_time_us(lambda: ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D),
                                                                   Hkv, mlen, gs, pl_, Sb, shared, workspace=wss,
-                                                                  status=st_sp), 50, stream)
+                                                                  status=st_sp))
+    t_shared_e = _event_time_us(lambda: ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D),
+                                                                    Hkv, mlen, gs, pl_, Sb, shared, workspace=wss,
+                                                                    status=st_sp), 50, stream)
     logical = int(ln.sum()) * Hkv * D * 2 * 2 + 2 * Sb * Hq_ * D * 2
     unique_blocks = len(set(tb[:, :int(ln.max()) // bs + 1].ravel().tolist()))
     sp_ok = int(st_sp.item()) == 0
@@ -405,11 +432,16 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     pc.close()
     return {
         "append_layers": {"layers": Lyr, "tokens": T, "bytes": append_b, "us": round(t_app, 2),
-                          "GB/s": gbs(append_b, t_app), "us_one_launch_per_layer": round(t_app1, 2)},
+                          "GB/s": gbs(append_b, t_app), "us_called_from_python": round(t_app_e, 2),
+                          "us_one_launch_per_layer": round(t_app1, 2)},
         "copy_blocks_layers": {"layers": Lyr, "pairs": pairs_n, "bytes": copy_b, "us": round(t_cp, 2),
-                               "GB/s": gbs(copy_b, t_cp), "us_one_launch_per_layer": round(t_cp1, 2)},
+                               "GB/s": gbs(copy_b, t_cp), "us_called_from_python": round(t_cp_e, 2),
+                               "us_one_launch_per_layer": round(t_cp1, 2)},
         "note": "bf16, 8 kv heads, head_dim 128, block 16; bytes = read + write of the moved K/V; "
-                "inputs smaller than L2 (the append's 67 MB, the copy's 268 MB straddles it)",
+                "us = device time per launch, replayed from a CUDA graph; us_called_from_python = "
+                "back-to-back calls through the binding (host dispatch bound); "
+                "us_one_launch_per_layer = the same work as one call per layer, from Python; "
+                "the append's 67 MB stay in L2 across launches, the copy's 268 MB straddle it",
         "prefill": {"prompts": S_, "tokens_per_prompt": n_, "q_heads": Hq_, "kv_heads": Hkv, "head_dim": D,
                     "us": round(t_pf, 1), "TFLOP/s": round(pf_tflops, 1),
                     "frac_of_bf16_peak": round(pf_tflops / bf16_peak, 4), "bf16_peak_tflops": bf16_peak,
@@ -418,6 +450,7 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
         "shared_prefix_decode": {"sequences": Sb, "shared_tokens": shared, "own_tokens": pref + own - shared,
                                  "logical_bytes": logical, "unique_kv_bytes": unique_blocks * Hkv * bs * D * 2 * 2,
                                  "us_pa_decode": round(t_plain, 2), "us_shared_prefix": round(t_shared, 2),
+                                 "us_shared_prefix_called_from_python": round(t_shared_e, 2),
                                  "logical_GB/s_pa_decode": gbs(logical, t_plain),
                                  "logical_GB/s_shared_prefix": gbs(logical, t_shared), "status_ok": sp_ok,
                                  "note": "the unique K/V fits in L2: logical bytes are what the tables name"},
