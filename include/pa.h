@@ -172,6 +172,10 @@ pa_status pa_copy_blocks_layers(void* k_cache, void* v_cache,
  * to finish a (sequence, kv head) merges them by log-sum-exp.
  * If a bounded device wait ever expires, the kernel stops early, the output
  * is undefined, and pa_workspace_error() reports PA_ERR_DEVICE_TIMEOUT.
+ * The tensor-core kernel is launched with programmatic stream serialisation:
+ * its set-up may overlap the tail of the kernel before it on the stream (the
+ * append signals this at its start), and it reads no input before that
+ * kernel has completed, so stream order holds as for any launch.
  * ---------------------------------------------------------------------- */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t block_size, pa_dtype dtype,
@@ -240,10 +244,12 @@ pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_stat
  * group j is [group_start[j], group_start[j+1]).  The first prefix_len[j]
  * tokens of every member are the same blocks: the first prefix_len[j] /
  * block_size entries of every member's table are equal.  A sequence that
- * shares nothing is a group of its own with prefix 0.  The call runs
+ * shares nothing is a group of its own with prefix 0.  The call runs, in one
+ * launch,
  *  (1) every group's queries (members x heads of a kv head, as the rows of
- *      dense 128-row tiles) against its prefix, split into partitions;
+ *      dense 128-row tiles) against its prefix, split into partitions, and
  *  (2) every member's own tokens [prefix_len, context_len);
+ * then, in a second launch that may start as the first drains,
  *  (3) a log-sum-exp merge of the partial results into out.
  *   q, out           device, [num_seqs][num_q_heads][128]; q bf16
  *   group_start      device, int32 [num_groups + 1], group_start[0] == 0,
@@ -260,7 +266,7 @@ pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_stat
  *                    PA_ERR_DEVICE_TIMEOUT if a bounded wait expired
  * Supported: bf16 K/V and q, head_dim 128, block_size 8..256, num_q_heads /
  * num_kv_heads in {1, 2, 4, 8, 16}; PA_ERR_UNSUPPORTED otherwise;
- * PA_ERR_WORKSPACE if the workspace is too small.  Three launches on stream.
+ * PA_ERR_WORKSPACE if the workspace is too small.  Two launches on stream.
  * ---------------------------------------------------------------------- */
 size_t    pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                                  int32_t num_kv_heads, int32_t num_groups,
