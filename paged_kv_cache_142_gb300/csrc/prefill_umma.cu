@@ -501,6 +501,68 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       }
       ptx::tmem_st32(dst, w);
     };
+    // An item's epilogue: its O row divided by the row sum and stored, once
+    // its last P.V (tile last_sc) has landed; then O is handed to the next
+    // item.  It runs after the next item's first softmax tile, so that P.V
+    // is usually done by then and the wait costs nothing.
+    auto epilogue = [&](const Item& eit, bool evalid, float em, float el, uint32_t last_sc) -> bool {
+      wait(&bars[kSFree + (last_sc & 1u)], (last_sc >> 1) & 1u, aborted);
+      aborted = __any_sync(0xffffffffu, aborted);
+      if (aborted) return false;
+      ptx::tc_fence_after();
+      const bool partial = p.mode != 0;  // shared-prefix decode: (max, sum, unnormalised O)
+      const float inv = partial ? 1.f : (evalid && el > 0.f ? 1.f / el : 0.f);
+      const int64_t prow = static_cast<int64_t>(eit.qb + eit.tok0 + trow) * p.num_q_heads + eit.kvh * G + g;
+      const int64_t orow = prow * 128;
+      const int64_t slot_rows = static_cast<int64_t>(eit.part) * p.num_seqs * p.num_q_heads;
+      if (partial && evalid) {
+        p.part_ml[(slot_rows + prow) * 2] = em;
+        p.part_ml[(slot_rows + prow) * 2 + 1] = el;
+      }
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32], vl[32];
+        ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
+        ptx::TmemLd<32>::run(tmem + lane_base + kColO + 128 + c * 32, vl);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
+        if (evalid && partial) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + (slot_rows + prow) * 128 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        } else if (evalid) {
+          if (p.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+              dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                   __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
+      return true;
+    };
+    bool pending = false;  // an item whose epilogue is still to run
+    Item pit{};
+    bool pvalid = false;
+    float pm = 0.f, pl = 0.f;
+    uint32_t psc = 0;
     for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
       Item it;
       if (!item_at(p, w, G, it)) continue;
@@ -577,60 +639,20 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bars[kPFull + b]);
         ++sc;
-      }
-      if (aborted) break;
-      // epilogue: O row / row sum, once the item's last P.V has landed
-      wait(&bars[kSFree + ((sc - 1u) & 1u)], ((sc - 1u) >> 1) & 1u, aborted);
-      aborted = __any_sync(0xffffffffu, aborted);
-      if (aborted) break;
-      ptx::tc_fence_after();
-      const bool partial = p.mode != 0;  // shared-prefix decode: (max, sum, unnormalised O)
-      const float inv = partial ? 1.f : (valid && l > 0.f ? 1.f / l : 0.f);
-      const int64_t prow = static_cast<int64_t>(it.qb + it.tok0 + trow) * p.num_q_heads + it.kvh * G + g;
-      const int64_t orow = prow * 128;
-      const int64_t slot_rows = static_cast<int64_t>(it.part) * p.num_seqs * p.num_q_heads;
-      if (partial && valid) {
-        p.part_ml[(slot_rows + prow) * 2] = m_ref;
-        p.part_ml[(slot_rows + prow) * 2 + 1] = l;
-      }
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32], vl[32];
-        ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
-        ptx::TmemLd<32>::run(tmem + lane_base + kColO + 128 + c * 32, vl);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
-        if (valid && partial) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + (slot_rows + prow) * 128 + c * 32);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        } else if (valid) {
-          if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c * 32);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t w4[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
-              dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                   __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
-          }
+        if (t == 0 && pending) {  // the previous item's epilogue, its P.V likely done
+          pending = false;
+          if (!epilogue(pit, pvalid, pm, pl, psc)) break;
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
+      if (aborted) break;
+      pending = true;
+      pit = it;
+      pvalid = valid;
+      pm = m_ref;
+      pl = l;
+      psc = sc - 1u;
     }
+    if (pending && !aborted) epilogue(pit, pvalid, pm, pl, psc);
   }
 
   // ============================ teardown ============================
