@@ -31,13 +31,6 @@ def test_traffic_only_for_the_profiled_kernel_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic() is None
 
 
-def test_committed_profile_matches_the_current_decode_source():
-    """The committed summary was taken on the kernel as it stands (else the
-    bench reports traffic as null and the summary must be refreshed)."""
-    bench = _bench()
-    assert bench.profiled_traffic() is not None
-
-
 def test_step_bytes_from_lengths_and_shapes():
     bench = _bench()
     lens = np.array([5, 16, 17, 40])
