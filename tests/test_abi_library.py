@@ -86,3 +86,23 @@ def test_argument_errors_return_before_any_launch(lib):
     rc = lib.pa_decode(None, 0, None, 2, 8, None, None, 8, 16, 4, 128, 1, None, 2, None, 64,
                        1.0, 0, None, 0, None)
     assert rc == L.PA_ERR_INVALID_ARG
+
+
+def test_plain_c_program_uses_the_host_calls(lib, tmp_path):
+    """include/pa.h is usable from C11 alone: a C program drives the block
+    allocator and SHA-256 through the library, with no Python in between."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from paged_kv_cache_142_gb300 import _lib as L
+    libdir = os.path.dirname(L.LIB_PATH)
+    exe = tmp_path / "c_abi_host"
+    here = os.path.dirname(os.path.abspath(__file__))
+    build = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(here, "..", "include"),
+                            os.path.join(here, "c_abi_host.c"), "-o", str(exe), "-L", libdir, "-lpa_gb300",
+                            f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stderr)
