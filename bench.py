@@ -12,10 +12,16 @@ Prints one JSON line (rank 0):
              read + write), timed with CUDA events over exactly K steps
   e2e        the same metric through the C ABI from pinned host buffers: per
              step the host allocator reserves the slots, tables/lens/q/new
-             K,V go host->device, the kernels run, the output comes back
+             K,V go host->device in one copy, the kernels run (a CUDA graph
+             per buffer set), the output comes back; the upload of the next
+             step and the download of the last overlap the kernels
   roofline   pa_decode's algorithmic bytes / its mean CUDA-event duration,
-             against the measured HBM copy bandwidth
+             against the measured HBM copy bandwidth; DRAM traffic from the
+             committed ncu summary while the kernel source is unchanged
   cpu_baseline  the fp64 oracle on a bounded sample, on the host
+  extras     the other rows' kernels on their own workloads: multi-layer
+             append and copy, paged prefill, shared-prefix decode, the MHA
+             and long-context decode configurations, prefix caching
 
 ``--impl reference`` times the oracle instead (the reference arm).
 Multi-GPU: data-parallel shards, one per rank.  Sequences are independent,
