@@ -39,3 +39,15 @@ def test_step_bytes_from_lengths_and_shapes():
     assert decode_b == int(lens.sum()) * Hkv * D * e * 2 + 2 * B * H * D * e
     # new K and V read and written, plus the int64 slot of each token
     assert append_b == B * Hkv * D * e * 2 * 2 + 8 * B
+
+
+def test_workloads_without_values_keep_lengths_and_free_lists():
+    """The bench's MHA and long-context extras draw their values on the
+    device; their lengths, pool and free-list order must be the parity
+    workloads' own."""
+    from paged_kv_cache_142_gb300 import workloads as W
+    for make in (lambda v: W.mha_bf16(values=v), lambda v: W.long_bf16(block_size=32, num_seqs=2, values=v)):
+        full, bare = make(True), make(False)
+        assert np.array_equal(full.context_lens, bare.context_lens)
+        assert np.array_equal(full.free_order, bare.free_order)
+        assert full.num_blocks == bare.num_blocks and bare.key_hist is None and bare.q is None
