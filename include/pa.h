@@ -68,7 +68,9 @@ const char* pa_version(void);
  *   k_cache[s / block_size][h][s % block_size][:] = key[t][h][:]
  *   v_cache[...same...]                             = value[t][h][:]
  * for every kv head h.  Negative slots (padding) are skipped; slots >=
- * num_blocks*block_size are skipped too (never written).
+ * num_blocks*block_size are skipped too (never written; the slots are in
+ * device memory, so they are not checked on the host, and
+ * pa_reshape_and_cache_checked below reports them).
  *
  *   key, value    device, [num_tokens][num_kv_heads][head_dim] of dtype
  *   slot_mapping  device, int64 [num_tokens]
@@ -92,16 +94,54 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_t
  * v_cache[src_j] (all kv heads, all block_size tokens), where
  * block_pairs[2j] = src_j and block_pairs[2j+1] = dst_j.
  *   block_pairs   device, int64 [num_pairs][2]
- * Precondition (not checked on the device): destinations are distinct and
- * none is also a source in the same call; then the result equals copying
- * from the state before the call.  Pairs naming a block outside
- * [0, num_blocks) are skipped.  num_pairs == 0 is a no-op.
+ * Pairs are valid when every block is in [0, num_blocks), the destinations
+ * are distinct and none is also a source in the same call (copy-on-write
+ * pairs always are); then the result equals copying from the state before
+ * the call.  The pairs live in device memory, so this call does not read or
+ * check them on the host: a pair naming a block outside the pool is skipped,
+ * and overlapping pairs give an undefined result for the blocks involved.
+ * pa_copy_blocks_checked reports invalid pairs instead.  num_pairs == 0 is
+ * a no-op.
  * ---------------------------------------------------------------------- */
 pa_status pa_copy_blocks(void* k_cache, void* v_cache,
                          int32_t num_blocks, int32_t block_size,
                          int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
                          const int64_t* block_pairs, int32_t num_pairs,
                          void* stream);
+
+/* ------------------------------------------------------------------------
+ * Checked append and copy (an opt-in validation mode for debugging) --
+ * [PA] "Block Table 如何工作": a slot is physical_block * block_size +
+ * offset, so a slot at or past num_blocks * block_size names no block of the
+ * pool; [PA] "支持块级共享": a copy-on-write copies a shared block to a fresh
+ * one, so its destinations are new blocks, distinct and never sources.
+ *
+ * Same arguments and result as pa_reshape_and_cache / pa_copy_blocks, plus
+ *   status   device int32, caller-zeroed (required, 4-byte aligned).  After
+ *            the call's work completes (stream order) it holds
+ *            PA_ERR_INVALID_ARG if anything was invalid, else it is unchanged.
+ * pa_reshape_and_cache_checked: a token whose slot is >= num_blocks *
+ *   block_size sets *status and is not written; every other token is
+ *   written as by pa_reshape_and_cache (negative slots are padding, skipped).
+ * pa_copy_blocks_checked: first validates every pair (a block outside
+ *   [0, num_blocks), a destination named twice, or a destination that is
+ *   also a source, itself included, sets *status), then copies only if
+ *   *status is still zero: on an invalid pair set no block is copied.  A
+ *   status left non-zero by an earlier call suppresses the copy too.  Two
+ *   launches on stream; the validation makes num_pairs^2 comparisons.
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache_checked(const void* key, const void* value, int32_t num_tokens,
+                                       const int64_t* slot_mapping,
+                                       void* k_cache, void* v_cache,
+                                       int32_t num_blocks, int32_t block_size,
+                                       int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                       int32_t* status, void* stream);
+
+pa_status pa_copy_blocks_checked(void* k_cache, void* v_cache,
+                                 int32_t num_blocks, int32_t block_size,
+                                 int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                 const int64_t* block_pairs, int32_t num_pairs,
+                                 int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
  * Multi-layer KV append and block copy -- [PA] "KV Cache 为什么难管理": a
@@ -210,7 +250,9 @@ pa_status pa_decode(void* out, pa_dtype out_dtype,
  * any stream capture.  Every call shares the one array and zeroes its
  * bookkeeping words first, so calls that overlap on the GPU (other streams,
  * other host threads) race and corrupt each other: issue them in one stream
- * order.  Device-side status (pa_workspace_error) is not reported. */
+ * order.  Device-side status (a table entry outside the pool, a length above
+ * max_context_len, a wait that timed out) goes to the array's error word,
+ * which pa_decode_no_alloc_error reads. */
 pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype,
                              const void* q, int32_t num_seqs, int32_t num_q_heads,
                              const void* k_cache, const void* v_cache,
@@ -220,6 +262,14 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype,
                              const int32_t* context_lens, int32_t max_context_len,
                              float scale, int32_t partition_tokens, void* stream);
 
+/* Device status of the pa_decode_no_alloc calls on the current device since
+ * the last call (each call clears the word first, so this reports the last
+ * one): synchronises `stream` (the stream the decode ran on), reads the
+ * scratch array's error word into *device_status (PA_OK,
+ * PA_ERR_INVALID_ARG or PA_ERR_DEVICE_TIMEOUT, as pa_workspace_error) and
+ * clears it.  Like pa_decode_no_alloc, it allocates nothing. */
+pa_status pa_decode_no_alloc_error(void* stream, int32_t* device_status);
+
 /* Partition size and CTA count pa_decode would use (host only; either out
  * pointer may be NULL). */
 pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -227,11 +277,25 @@ pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
                          int32_t max_context_len, int32_t partition_tokens,
                          int32_t* partition_tokens_out, int32_t* num_ctas_out);
 
+/* Testing hook for the timeout path, not for production use.  With ns > 0,
+ * every pa_decode launch of the tensor-core kernel (bf16, head_dim 128) made
+ * after this call in this process has its compute warps first wait for an
+ * event that never comes, giving up after ns nanoseconds (at most 2 s); 0
+ * turns the hook off.  A CTA whose wait gives up raises its stop word: every
+ * role stops, copies and tensor-core work already issued are waited for,
+ * tensor memory is freed, the output is left undefined, and
+ * PA_ERR_DEVICE_TIMEOUT reaches the host through pa_workspace_error.  The
+ * workspace must be zeroed again (pa_workspace_init) before its next use.
+ * The same stop path serves any real wait that runs out its 2 s limit. */
+void pa_test_stall_decode(uint64_t ns);
+
 /* Zero a decode workspace (enqueued on `stream`). */
 pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then reads the workspace's device error word into
- * *device_status (PA_OK or PA_ERR_DEVICE_TIMEOUT) and clears it. */
+ * *device_status (PA_OK; PA_ERR_INVALID_ARG for a table entry outside the
+ * pool or a context length outside [0, max_context_len]; or
+ * PA_ERR_DEVICE_TIMEOUT) and clears it. */
 pa_status pa_workspace_error(void* workspace, void* stream, int32_t* device_status);
 
 /* ------------------------------------------------------------------------

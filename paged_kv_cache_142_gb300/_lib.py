@@ -35,6 +35,8 @@ SIGNATURES = {
     "pa_version": (C.c_char_p, []),
     "pa_reshape_and_cache": (i32, [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_copy_blocks": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, i32, vp]),
+    "pa_reshape_and_cache_checked": (i32, [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "pa_copy_blocks_checked": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp]),
     "pa_reshape_and_cache_layers": (i32, [vp, vp, i64, i32, i32, vp, vp, vp, i64, i32, i32, i32,
                                           i32, i32, vp]),
     "pa_copy_blocks_layers": (i32, [vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, i32, vp]),
@@ -48,8 +50,10 @@ SIGNATURES = {
                         C.c_float, i32, vp, C.c_size_t, vp]),
     "pa_decode_no_alloc": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32,
                                  vp, i32, C.c_float, i32, vp]),
+    "pa_decode_no_alloc_error": (i32, [vp, P_i32]),
     "pa_decode_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, P_i32, P_i32]),
     "pa_workspace_init": (i32, [vp, C.c_size_t, vp]),
+    "pa_test_stall_decode": (None, [C.c_uint64]),
     "pa_workspace_error": (i32, [vp, vp, P_i32]),
     "pa_alloc_create": (i32, [i32, i32, P_i32, C.POINTER(vp)]),
     "pa_alloc_destroy": (None, [vp]),

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "decode.cuh"
@@ -19,6 +20,28 @@ bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInf
   return dtype_bf16 ? decode_info_bf16(head_dim, group, info)
                     : decode_info_f32(head_dim, group, info);
 }
+
+constexpr int64_t kSmCountDefault = 152;  // GB300; used only when no device can be queried
+
+// SMs of the current device, which shape the default partition sizes (host
+// planning calls also work without a GPU, with the GB300's count).
+int64_t device_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();  // clear the query's error
+    return kSmCountDefault;
+  }
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return kSmCountDefault;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 }  // namespace pa
 
 namespace {
@@ -26,16 +49,18 @@ namespace {
 using pa::DecodeKernelInfo;
 using pa::DecodeParams;
 
+// Timeout-path test hook (pa_test_stall_decode): 0 = off.
+std::atomic<uint64_t> g_test_stall_ns{0};
+
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kDefaultPartTokens = 256;
 constexpr int32_t kMaxLayers = 32767;  // grid y of the copy kernel holds 2 * layers
-constexpr int64_t kSmCountHint = 152;  // GB300 SMs; only shapes the default partition size
-
 int dtype_bytes(pa_dtype d) {
   return d == PA_DTYPE_F32 ? 4 : (d == PA_DTYPE_BF16 ? 2 : 0);
 }
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -100,7 +125,8 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   if (pl->umma) {
     def_pt = max_context_len > 4096 ? 4096 : 2048;
     const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
-    while (def_pt > 256 && units * ceil_div(max_context_len, def_pt) < 2 * kSmCountHint) def_pt /= 2;
+    const int64_t sms = pa::device_sm_count();
+    while (def_pt > 256 && units * ceil_div(max_context_len, def_pt) < 2 * sms) def_pt /= 2;
   }
   int64_t pt = round_up(partition_tokens > 0 ? partition_tokens : def_pt, gran);
   while (ceil_div(max_context_len, pt) > pt / 2) pt *= 2;
@@ -293,12 +319,15 @@ const char* pa_status_string(pa_status s) {
 
 const char* pa_version(void) { return "pa_gb300 1.0 sm_103a"; }
 
-pa_status pa_reshape_and_cache_layers(const void* key, const void* value, int64_t kv_layer_stride,
+}  // extern "C"
+
+namespace {
+pa_status reshape_and_cache_impl(const void* key, const void* value, int64_t kv_layer_stride,
                                       int32_t num_layers, int32_t num_tokens,
                                       const int64_t* slot_mapping, void* k_cache, void* v_cache,
                                       int64_t cache_layer_stride, int32_t num_blocks,
                                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
-                                      pa_dtype dtype, void* stream) {
+                                      pa_dtype dtype, int32_t* status, void* stream) {
   pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
   if (num_tokens < 0 || num_layers < 1 || num_layers > kMaxLayers) return PA_ERR_INVALID_ARG;
@@ -310,14 +339,29 @@ pa_status pa_reshape_and_cache_layers(const void* key, const void* value, int64_
     return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (status && !aligned4(status)) return PA_ERR_INVALID_ARG;
   if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
     return PA_ERR_INVALID_ARG;
   const int32_t row = head_dim * static_cast<int32_t>(e);
   cudaError_t err = pa::launch_reshape_and_cache(
       key, value, num_layers > 1 ? kv_layer_stride * e : 0, num_layers, num_tokens, slot_mapping,
       k_cache, v_cache, num_layers > 1 ? cache_layer_stride * e : 0, num_blocks, block_size,
-      num_kv_heads, row, static_cast<cudaStream_t>(stream));
+      num_kv_heads, row, status, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+pa_status pa_reshape_and_cache_layers(const void* key, const void* value, int64_t kv_layer_stride,
+                                      int32_t num_layers, int32_t num_tokens,
+                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                      int64_t cache_layer_stride, int32_t num_blocks,
+                                      int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                      pa_dtype dtype, void* stream) {
+  return reshape_and_cache_impl(key, value, kv_layer_stride, num_layers, num_tokens, slot_mapping,
+                                k_cache, v_cache, cache_layer_stride, num_blocks, block_size,
+                                num_kv_heads, head_dim, dtype, nullptr, stream);
 }
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_tokens,
@@ -329,10 +373,25 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, int32_t num_t
                                      stream);
 }
 
-pa_status pa_copy_blocks_layers(void* k_cache, void* v_cache, int64_t cache_layer_stride,
+pa_status pa_reshape_and_cache_checked(const void* key, const void* value, int32_t num_tokens,
+                                       const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                       int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                       int32_t head_dim, pa_dtype dtype, int32_t* status,
+                                       void* stream) {
+  if (!status) return PA_ERR_INVALID_ARG;
+  return reshape_and_cache_impl(key, value, 0, 1, num_tokens, slot_mapping, k_cache, v_cache, 0,
+                                num_blocks, block_size, num_kv_heads, head_dim, dtype, status,
+                                stream);
+}
+
+}  // extern "C"
+
+namespace {
+pa_status copy_blocks_impl(void* k_cache, void* v_cache, int64_t cache_layer_stride,
                                 int32_t num_layers, int32_t num_blocks, int32_t block_size,
                                 int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
-                                const int64_t* block_pairs, int32_t num_pairs, void* stream) {
+                                const int64_t* block_pairs, int32_t num_pairs, int32_t* status,
+                                void* stream) {
   pa_status st = check_cache_shape(num_blocks, block_size, num_kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
   if (num_pairs < 0 || num_layers < 1 || num_layers > kMaxLayers) return PA_ERR_INVALID_ARG;
@@ -343,12 +402,33 @@ pa_status pa_copy_blocks_layers(void* k_cache, void* v_cache, int64_t cache_laye
   if (num_pairs == 0) return PA_OK;
   if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  if (status && !aligned4(status)) return PA_ERR_INVALID_ARG;
   const int64_t block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * e;
   cudaError_t err = pa::launch_copy_blocks(k_cache, v_cache,
                                            num_layers > 1 ? cache_layer_stride * e : 0, num_layers,
-                                           num_blocks, block_bytes, block_pairs, num_pairs,
+                                           num_blocks, block_bytes, block_pairs, num_pairs, status,
                                            static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+pa_status pa_copy_blocks_layers(void* k_cache, void* v_cache, int64_t cache_layer_stride,
+                                int32_t num_layers, int32_t num_blocks, int32_t block_size,
+                                int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                const int64_t* block_pairs, int32_t num_pairs, void* stream) {
+  return copy_blocks_impl(k_cache, v_cache, cache_layer_stride, num_layers, num_blocks, block_size,
+                          num_kv_heads, head_dim, dtype, block_pairs, num_pairs, nullptr, stream);
+}
+
+pa_status pa_copy_blocks_checked(void* k_cache, void* v_cache, int32_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                 pa_dtype dtype, const int64_t* block_pairs, int32_t num_pairs,
+                                 int32_t* status, void* stream) {
+  if (!status) return PA_ERR_INVALID_ARG;
+  return copy_blocks_impl(k_cache, v_cache, 0, 1, num_blocks, block_size, num_kv_heads, head_dim,
+                          dtype, block_pairs, num_pairs, status, stream);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
@@ -448,7 +528,7 @@ namespace {
 int64_t cascade_part_tokens(int64_t max_prefix, int64_t items_per_part) {
   // enough (prefix partition, tile, group, kv head) items for every SM twice,
   // partitions of at least 256 keys, in 128-key multiples
-  int64_t parts = (2 * kSmCountHint + items_per_part - 1) / (items_per_part > 0 ? items_per_part : 1);
+  int64_t parts = (2 * pa::device_sm_count() + items_per_part - 1) / (items_per_part > 0 ? items_per_part : 1);
   if (parts < 1) parts = 1;
   int64_t pt = (max_prefix + parts - 1) / parts;
   pt = round_up(pt < 256 ? 256 : pt, 128);
@@ -635,6 +715,7 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
   p.ws_counters = reinterpret_cast<int32_t*>(ws + pl.ws_counters);
   p.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   p.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
+  p.test_stall_ns = g_test_stall_ns.load(std::memory_order_relaxed);
 
   cudaError_t e;
   if (pl.umma) {
@@ -671,6 +752,10 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
                          args, static_cast<size_t>(pl.smem), static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+void pa_test_stall_decode(uint64_t ns) {
+  g_test_stall_ns.store(ns < pa::kWaitLimitNs ? ns : pa::kWaitLimitNs, std::memory_order_relaxed);
 }
 
 pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -718,6 +803,27 @@ void* g_noalloc_addr[kNoAllocMaxDevices] = {};
 
 }  // namespace
 
+namespace {
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (the host-side symbol is only a
+// stand-in, not a device address).
+pa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
 extern "C" pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
                                         int32_t num_seqs, int32_t num_q_heads,
                                         const void* k_cache, const void* v_cache,
@@ -726,33 +832,25 @@ extern "C" pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const voi
                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
                                         const int32_t* context_lens, int32_t max_context_len,
                                         float scale, int32_t partition_tokens, void* stream) {
-  // Device address of the scratch array on the current device, looked up once
-  // per device (the host-side symbol is only a stand-in, not a device address).
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return PA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
-      g_noalloc_addr[dev] = p;
-    }
-    scratch = g_noalloc_addr[dev];
-  }
-  // Plan; with automatic partitions, enlarge them until the scratch fits.
+  pa_status st = noalloc_scratch(&scratch);
+  if (st != PA_OK) return st;
+  // Plan; with automatic partitions, enlarge them until the scratch fits.  A
+  // plan that fails while partitions are being enlarged (partitions past the
+  // planner's limit, or shared memory for them) means the scratch is too small
+  // for this batch.
   Plan pl;
   int32_t pt = partition_tokens;
-  pa_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
-                           max_context_len, pt, &pl);
+  st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                 max_context_len, pt, &pl);
   if (st != PA_OK) return st;
   while (pl.ws_total > kNoAllocScratchBytes) {
-    if (partition_tokens > 0 || pl.max_parts == 1) return PA_ERR_WORKSPACE;
+    if (partition_tokens > 0 || pl.max_parts == 1 || pl.part_tokens > (1 << 29))
+      return PA_ERR_WORKSPACE;
     pt = pl.part_tokens * 2;
-    st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
-                   max_context_len, pt, &pl);
-    if (st != PA_OK) return st;
+    if (make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                  max_context_len, pt, &pl) != PA_OK)
+      return PA_ERR_WORKSPACE;
   }
   if (num_seqs == 0) return PA_OK;
   // The array keeps the previous call's contents: zero the error word and the
@@ -762,4 +860,12 @@ extern "C" pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const voi
   return pa_decode(out, out_dtype, q, num_seqs, num_q_heads, k_cache, v_cache, num_blocks,
                    block_size, num_kv_heads, head_dim, dtype, block_tables, max_blocks_per_seq,
                    context_lens, max_context_len, scale, pt, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" pa_status pa_decode_no_alloc_error(void* stream, int32_t* device_status) {
+  if (!device_status) return PA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const pa_status st = noalloc_scratch(&scratch);
+  if (st != PA_OK) return st;
+  return pa_workspace_error(scratch, stream, device_status);
 }

@@ -54,7 +54,13 @@ struct DecodeParams {
   int32_t* ws_counters;
   float* ws_ml;
   float* ws_o;
+  // timeout-path test hook of the tensor-core kernel (0 = off): its compute
+  // warps first wait this long for an event that never comes, then give up
+  uint64_t test_stall_ns;
 };
+
+// SMs of the current device (152, the GB300's, when none can be queried).
+int64_t device_sm_count();
 
 // Per (dtype, head_dim, group) kernel entry: shared memory need and launch.
 struct DecodeKernelInfo {
@@ -105,16 +111,18 @@ int prefill_umma_smem_bytes();
 cudaError_t launch_cascade_merge(const PrefillParams& p, cudaStream_t stream);
 
 // Cache ops over num_layers layers of one pool (layer strides in bytes,
-// multiples of 16); one layer is num_layers == 1.
+// multiples of 16); one layer is num_layers == 1.  status == nullptr: the
+// unchecked calls; else the checked mode (see cache_ops.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kv_layer_bytes,
                                      int32_t num_layers, int32_t num_tokens,
                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
                                      int64_t cache_layer_bytes, int32_t num_blocks,
                                      int32_t block_size, int32_t num_kv_heads, int32_t row_bytes,
-                                     cudaStream_t stream);
+                                     int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t cache_layer_bytes,
                                int32_t num_layers, int32_t num_blocks, int64_t block_bytes,
-                               const int64_t* pairs, int32_t num_pairs, cudaStream_t stream);
+                               const int64_t* pairs, int32_t num_pairs, int32_t* status,
+                               cudaStream_t stream);
 
 }  // namespace pa

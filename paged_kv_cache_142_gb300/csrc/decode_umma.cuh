@@ -76,7 +76,7 @@ __host__ __device__ constexpr int umma_small_bytes(int G) { return G >= 8 ? 1280
 constexpr int kUmmaGroupBars = 16;
 constexpr int kUmmaQueue = 8;            // per-group item queue depth
 constexpr int kUmmaQueueReaders = 9;     // V stream, 2 Q.K and 2 P.V warps, a group's 4 compute warps
-constexpr int kUmmaBarriers = 6 * kUmmaMaxStages + 2 * kUmmaGroupBars + 4 + 4 * kUmmaQueue;
+constexpr int kUmmaBarriers = 6 * kUmmaMaxStages + 2 * kUmmaGroupBars + 4 + 4 * kUmmaQueue + 1;
 
 __host__ __device__ constexpr int umma_p_bytes(int G) { return G <= 8 ? 4096 : 8192; }
 
@@ -101,6 +101,7 @@ constexpr int kDrainQK = 6 * kUmmaMaxStages + 2 * kUmmaGroupBars;   // [group]
 constexpr int kDrainPV = kDrainQK + 2;                               // [group]
 constexpr int kItemFull = kDrainPV + 2;                   // [group][kUmmaQueue]
 constexpr int kItemEmpty = kItemFull + 2 * kUmmaQueue;    // [group][kUmmaQueue]
+constexpr int kNever = kItemEmpty + 2 * kUmmaQueue;       // no role ever arrives (timeout-path test)
 
 struct Item {
   int seq, kvh, part, len, t0, ntok, nparts;
@@ -337,9 +338,26 @@ struct NoOp {
   __device__ __forceinline__ void operator()(int, const Item&) const {}
 };
 
-// bounded wait; once a role has given up, later waits are skipped
-__device__ __forceinline__ void wait(uint64_t* bar, uint32_t parity, bool& aborted) {
-  if (!aborted && !ptx::mbar_wait(bar, parity, kWaitLimitNs)) aborted = true;
+// Bounded wait; once a role has given up, its later waits are skipped.
+// `stop` is the CTA's shared stop word: a role that gives up raises it, and
+// every role still spinning gives up at once rather than after its own limit.
+__device__ __forceinline__ void wait(uint64_t* bar, uint32_t parity, bool& aborted,
+                                     volatile int* stop, uint64_t limit_ns = kWaitLimitNs) {
+  if (aborted || ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::global_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*stop || ptx::global_ns() - t0 > limit_ns) {
+      aborted = true;
+      *stop = 1;
+      return;
+    }
+  }
+}
+
+// Wait for work already issued (copies, MMAs) to finish before the CTA
+// exits: bounded by the default limit and not cut short by the stop word.
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  return ptx::mbar_wait(bar, parity, kWaitLimitNs);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -385,9 +403,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kUmmaBarriers);
   // [0] a streaming or MMA role gave up, [1..2] group merges its item,
-  // [3..4] group gave up
+  // [3..4] group gave up, [5] the stop word (some role gave up)
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* warp_sums = const_cast<int*>(flags) + 5;   // one int per warp
+  volatile int* stop = flags + 5;
+  int* warp_sums = const_cast<int*>(flags) + 6;   // one int per warp
   int32_t* tbl = reinterpret_cast<int32_t*>(smem + p.off_tbl);  // [K/V stream][group][tbl_stride]
   int32_t* lens = reinterpret_cast<int32_t*>(smem + p.off_lens);
   int32_t* prefix_full = reinterpret_cast<int32_t*>(smem + p.off_prefix);
@@ -433,7 +452,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       ptx::mbar_init(&bars[kItemFull + q], 1);
       ptx::mbar_init(&bars[kItemEmpty + q], kUmmaQueueReaders);
     }
-    for (int i = 0; i < 5; ++i) flags[i] = 0;
+    ptx::mbar_init(&bars[kNever], 1);
+    for (int i = 0; i < 6; ++i) flags[i] = 0;
     ptx::mbar_init_fence();
   }
   if (warp == 1) {
@@ -459,7 +479,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     int w = -1;
     if (lane == 0) {
       const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
-      wait(&bars[kItemFull + slot], (k / kUmmaQueue) & 1u, aborted);
+      wait(&bars[kItemFull + slot], (k / kUmmaQueue) & 1u, aborted, stop);
       if (!aborted) w = queue[slot];
       ptx::mbar_arrive(&bars[kItemEmpty + slot]);
     }
@@ -490,7 +510,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       int w = -1;
       if (lane == 0) {
         const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
-        wait(&bars[kItemEmpty + slot], ((k / kUmmaQueue) & 1u) ^ 1u, aborted);
+        wait(&bars[kItemEmpty + slot], ((k / kUmmaQueue) & 1u) ^ 1u, aborted, stop);
         if (!aborted) {
           w = atomicAdd(item_counter, 1);
           if (w >= ctx.total) w = -1;
@@ -506,7 +526,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     Stream st;
     st.init(ctx, next_w, NoOp{});
     int slot = 0;
-    uint32_t wrap = 0;  // fills of each slot so far: full copy wrap & 1, empty parity
+    uint32_t wrap = 0;   // fills of each slot so far: full copy wrap & 1, empty parity
+    uint32_t nfill = 0;  // ring fills whose copies were issued (fill n: slot n % NS)
+    uint32_t qfill0 = 0, qfill1 = 0;  // query fills issued per group (K stream)
     Rec r;
     while (!aborted && st.next(ctx, r, next_w, NoOp{})) {
       int32_t* gtbl = slice(r.g);
@@ -518,12 +540,16 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         __syncwarp();
         if (!is_v && lane == 0) {
           uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
-          wait(&gb[kQEmpty], (r.qi & 1u) ^ 1u, aborted);
-          ptx::mbar_arrive_expect_tx(&gb[kQFull], 2u * G * 128u);
-          unsigned char* qd = qbuf + r.g * kUmmaQBytes;
-          for (int h = 0; h < 2; ++h)
-            ptx::tma_load_2d(qd + h * 2048, &tm_q, 64 * h, r.it.seq * p.num_q_heads + r.it.kvh * G,
-                             &gb[kQFull], pol_q);
+          wait(&gb[kQEmpty], (r.qi & 1u) ^ 1u, aborted, stop);
+          if (!aborted) {
+            ptx::mbar_arrive_expect_tx(&gb[kQFull], 2u * G * 128u);
+            unsigned char* qd = qbuf + r.g * kUmmaQBytes;
+            for (int h = 0; h < 2; ++h)
+              ptx::tma_load_2d(qd + h * 2048, &tm_q, 64 * h, r.it.seq * p.num_q_heads + r.it.kvh * G,
+                               &gb[kQFull], pol_q);
+            if (r.g) qfill1 = r.qi + 1;
+            else qfill0 = r.qi + 1;
+          }
         }
       }
       // this lane's block of the tile (lanes < nbox)
@@ -542,19 +568,34 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       }
       uint64_t* fb = &full[(wrap & 1u) * kUmmaMaxStages + slot];
       if (lane == 0) {
-        wait(&empty[slot], (wrap & 1u) ^ 1u, aborted);
-        ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nbox * box_rows * 256));
+        wait(&empty[slot], (wrap & 1u) ^ 1u, aborted, stop);
+        if (!aborted) ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nbox * box_rows * 256));
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
-      if (!aborted && lane < nbox) {
+      if (aborted) break;
+      if (lane < nbox) {
         unsigned char* dst = ring + slot * kUmmaTileBytes + lane * box_rows * 256;
         ptx::tma_load_4d(dst, tm, 0, 0, 0, row >> 3, fb, pol_kv);
       }
+      ++nfill;
       __syncwarp();
       if (++slot == NS) {
         slot = 0;
         ++wrap;
       }
+    }
+    if (lane == 0 && (aborted || *stop)) {
+      // The copies this warp issued must land before the CTA exits: wait for
+      // the last fill of every slot (earlier fills of a slot completed before
+      // its next fill was issued) and, on the K stream, each group's last
+      // query fill.
+      const uint32_t first = nfill > static_cast<uint32_t>(NS) ? nfill - NS : 0u;
+      for (uint32_t n = first; n < nfill; ++n) {
+        const uint32_t s = n % NS, w = n / NS;
+        drain_wait(&full[(w & 1u) * kUmmaMaxStages + s], (w >> 1) & 1u);
+      }
+      if (!is_v && qfill0 > 0) drain_wait(&bars[kGroup0 + kQFull], (qfill0 - 1u) & 1u);
+      if (!is_v && qfill1 > 0) drain_wait(&bars[kGroup0 + kUmmaGroupBars + kQFull], (qfill1 - 1u) & 1u);
     }
   } else if (warp == 1 || warp == 12) {
     // ============================ Q.K^T issue ============================
@@ -564,7 +605,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       constexpr uint32_t kIdQK = ptx::idesc_bf16_f32(128, 16, 0, 0);
       auto read_one = [&](int g, uint32_t k) -> int {
         const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
-        wait(&bars[kItemFull + slot], (k / kUmmaQueue) & 1u, aborted);
+        wait(&bars[kItemFull + slot], (k / kUmmaQueue) & 1u, aborted, stop);
         const int w = aborted ? -1 : queue[slot];
         ptx::mbar_arrive(&bars[kItemEmpty + slot]);
         return w;
@@ -584,9 +625,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
         const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
-        if (r.j == 0) wait(&gb[kQFull], r.qi & 1u, aborted);
-        wait(&bars[kKFull + (kwrap & 1u) * kUmmaMaxStages + kslot], (kwrap >> 1) & 1u, aborted);
-        wait(&gb[kSEmpty + b], ph ^ 1u, aborted);
+        if (r.j == 0) wait(&gb[kQFull], r.qi & 1u, aborted, stop);
+        wait(&bars[kKFull + (kwrap & 1u) * kUmmaMaxStages + kslot], (kwrap >> 1) & 1u, aborted, stop);
+        wait(&gb[kSEmpty + b], ph ^ 1u, aborted, stop);
+        if (aborted) break;  // nothing is issued or released past a wait that gave up
         ptx::tc_fence_after();
         const unsigned char* kt = kring + kslot * kUmmaTileBytes;
         const unsigned char* qt = qbuf + r.g * kUmmaQBytes;
@@ -608,9 +650,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       }
       // nothing may be in flight when tensor memory is freed
       ptx::umma_commit(&bars[kDrainQK + my_g]);
-      bool drain_aborted = false;
-      wait(&bars[kDrainQK + my_g], 0, drain_aborted);
-      if (aborted || drain_aborted) flags[0] = 1;
+      const bool drained = drain_wait(&bars[kDrainQK + my_g], 0);
+      if (aborted || !drained) flags[0] = 1;
     }
     __syncwarp();
   } else if (warp == 11 || warp == 13) {
@@ -640,9 +681,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       const uint32_t b = r.ug & 1u, ph = (r.ug >> 1) & 1u;
       unsigned char* vt = vring + vslot * kUmmaTileBytes;
       if (lane == 0) {
-        wait(&bars[kVFull + (vwrap & 1u) * kUmmaMaxStages + vslot], (vwrap >> 1) & 1u, aborted);
-        wait(&gb[kPFull + b], ph, aborted);
-        wait(&gb[kOEmpty + b], ph ^ 1u, aborted);
+        wait(&bars[kVFull + (vwrap & 1u) * kUmmaMaxStages + vslot], (vwrap >> 1) & 1u, aborted, stop);
+        wait(&gb[kPFull + b], ph, aborted, stop);
+        wait(&gb[kOEmpty + b], ph ^ 1u, aborted, stop);
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
       if (aborted) break;
@@ -677,9 +718,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     }
     if (lane == 0) {
       ptx::umma_commit(&bars[kDrainPV + my_g]);
-      bool drain_aborted = false;
-      wait(&bars[kDrainPV + my_g], 0, drain_aborted);
-      if (aborted || drain_aborted) flags[0] = 1;
+      const bool drained = drain_wait(&bars[kDrainPV + my_g], 0);
+      if (aborted || !drained) flags[0] = 1;
     }
     __syncwarp();
   } else {
@@ -738,7 +778,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           l_thr[g] = 0.f;
         }
       }
-      wait(&gb[kSFull + b], ph, aborted);
+      wait(&gb[kSFull + b], ph, aborted, stop);
       ptx::tc_fence_after();
       uint32_t sr[G];
       ptx::TmemLd<G>::run(tmem + lane_base + (cg * 2 + b) * 16, sr);
@@ -808,7 +848,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       uint32_t wp[NP / 2];
 #pragma unroll
       for (int k = 0; k < NP / 2; ++k) wp[k] = pc[2 * k] | (pc[2 * k + 1] << 16);
-      wait(&gb[kPEmpty + b], ph ^ 1u, aborted);
+      wait(&gb[kPEmpty + b], ph ^ 1u, aborted, stop);
       unsigned char* prow = gp + b * PB + (r >> 3) * (PGRP * 128) + (r & 7) * 16;
 #pragma unroll
       for (int c = 0; c < PGRP; ++c)
@@ -936,7 +976,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     auto accumulate = [&](const Rec& t) {
       const uint32_t b = t.ug & 1u, ph = (t.ug >> 1) & 1u;
-      wait(&gb[kOFull + b], ph, aborted);
+      wait(&gb[kOFull + b], ph, aborted, stop);
       ptx::tc_fence_after();
       uint32_t orr[NP];
       ptx::TmemLd<NP>::run(tmem + lane_base + 64 + (cg * 2 + b) * NP, orr);
@@ -952,6 +992,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       if (t.j == t.nt - 1) epilogue(t);
     };
 
+    // timeout-path test hook: wait, with a short limit, for an event that
+    // never comes, so the group gives up and the CTA takes its stop path
+    if (p.test_stall_ns) wait(&bars[kNever], 0, aborted, stop, p.test_stall_ns);
     // this group's items only, in queue order
     GroupIter gi;
     gi.k = gi.items = 0;
@@ -994,7 +1037,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
   if (tid == 0) {
-    if (flags[0] || flags[3] || flags[4]) atomicExch(p.ws_err, kDevErrTimeout);
+    if (flags[0] || flags[3] || flags[4] || *stop) atomicExch(p.ws_err, kDevErrTimeout);
     // the last CTA to finish returns the item counter to zero for the next call
     __threadfence();
     if (atomicAdd(done_counter, 1) == static_cast<int>(gridDim.x) - 1) {

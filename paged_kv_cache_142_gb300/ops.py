@@ -40,39 +40,73 @@ def _need(cond: bool, msg: str) -> None:
         raise ValueError(msg)
 
 
+def _on_current_device(*tensors) -> None:
+    """The library launches on the current device (and its default stream),
+    so every tensor handed to it must live there."""
+    dev = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            _need(t.device.index == dev, f"tensor on cuda:{t.device.index} but the current device is "
+                  f"cuda:{dev}: call inside torch.cuda.device(...) of the tensors' device")
+
+
 def _cache_dims(k_cache: torch.Tensor, v_cache: torch.Tensor):
     _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [NB, Hkv, bs, D]")
     _need(k_cache.dtype == v_cache.dtype, "K and V caches must share a dtype")
     _need(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
     _need(k_cache.is_cuda and v_cache.is_cuda, "caches must be CUDA tensors")
+    _on_current_device(k_cache, v_cache)
     return k_cache.shape
 
 
 # --------------------------------------------------------------------------
 # device calls
 # --------------------------------------------------------------------------
-def pa_reshape_and_cache(key, value, slot_mapping, k_cache, v_cache, stream=None) -> None:
-    """Write key/value ``[T, Hkv, D]`` into the cache slots ``slot_mapping[T]``."""
+def pa_reshape_and_cache(key, value, slot_mapping, k_cache, v_cache, stream=None, status=None) -> None:
+    """Write key/value ``[T, Hkv, D]`` into the cache slots ``slot_mapping[T]``.
+    ``status`` (a zeroed CUDA int32 tensor): the checked call, which reports
+    slots past the pool there (pa_reshape_and_cache_checked)."""
     NB, Hkv, bs, D = _cache_dims(k_cache, v_cache)
+    _on_current_device(key, value, slot_mapping, status)
     T = key.shape[0]
     _need(key.shape == (T, Hkv, D) and value.shape == key.shape, "key/value must be [T, Hkv, D]")
     _need(key.dtype == k_cache.dtype and value.dtype == k_cache.dtype, "key/value dtype != cache dtype")
     _need(key.is_contiguous() and value.is_contiguous(), "key/value must be contiguous")
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T and slot_mapping.is_cuda,
           "slot_mapping must be a CUDA int64 tensor of num_tokens entries")
+    if status is not None:
+        _need(status.dtype == torch.int32 and status.is_cuda and status.numel() >= 1,
+              "status must be a CUDA int32 tensor")
+        L.check(_LIB.pa_reshape_and_cache_checked(
+            key.data_ptr(), value.data_ptr(), T, slot_mapping.data_ptr(), k_cache.data_ptr(),
+            v_cache.data_ptr(), NB, bs, Hkv, D, dtype_code(k_cache.dtype), status.data_ptr(),
+            _stream(stream)), "pa_reshape_and_cache_checked")
+        return
     L.check(_LIB.pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), T, slot_mapping.data_ptr(),
                                       k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
                                       dtype_code(k_cache.dtype), _stream(stream)),
             "pa_reshape_and_cache")
 
 
-def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
-    """cache[dst] = cache[src] for every row (src, dst) of ``block_pairs``."""
+def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None, status=None) -> None:
+    """cache[dst] = cache[src] for every row (src, dst) of ``block_pairs``.
+    ``status`` (a zeroed CUDA int32 tensor): the checked call, which validates
+    the pairs first and copies nothing if any is invalid
+    (pa_copy_blocks_checked)."""
     NB, Hkv, bs, D = _cache_dims(k_cache, v_cache)
+    _on_current_device(block_pairs, status)
     n = block_pairs.shape[0] if block_pairs.numel() else 0
     if n:
         _need(block_pairs.dtype == torch.int64 and block_pairs.is_cuda and block_pairs.is_contiguous()
               and block_pairs.shape == (n, 2), "block_pairs must be a contiguous CUDA int64 [n, 2]")
+    if status is not None:
+        _need(status.dtype == torch.int32 and status.is_cuda and status.numel() >= 1,
+              "status must be a CUDA int32 tensor")
+        L.check(_LIB.pa_copy_blocks_checked(k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
+                                            dtype_code(k_cache.dtype), block_pairs.data_ptr() if n else None,
+                                            n, status.data_ptr(), _stream(stream)),
+                "pa_copy_blocks_checked")
+        return
     L.check(_LIB.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
                                 dtype_code(k_cache.dtype), block_pairs.data_ptr() if n else None, n,
                                 _stream(stream)),
@@ -93,6 +127,7 @@ def pa_reshape_and_cache_layers(key, value, slot_mapping, k_cache, v_cache, stre
     """Every layer at once: key/value ``[L, T, Hkv, D]`` into the caches
     ``[L, NB, Hkv, bs, D]`` at ``slot_mapping[T]`` (the same slots in every layer)."""
     Lyr, NB, Hkv, bs, D = _layer_cache_dims(k_cache, v_cache)
+    _on_current_device(k_cache, v_cache, key, value, slot_mapping)
     T = key.shape[1]
     _need(key.shape == (Lyr, T, Hkv, D) and value.shape == key.shape, "key/value must be [L, T, Hkv, D]")
     _need(key.dtype == k_cache.dtype and value.dtype == k_cache.dtype, "key/value dtype != cache dtype")
@@ -109,6 +144,7 @@ def pa_reshape_and_cache_layers(key, value, slot_mapping, k_cache, v_cache, stre
 def pa_copy_blocks_layers(k_cache, v_cache, block_pairs, stream=None) -> None:
     """cache[l, dst] = cache[l, src] for every layer l and row (src, dst) of ``block_pairs``."""
     Lyr, NB, Hkv, bs, D = _layer_cache_dims(k_cache, v_cache)
+    _on_current_device(k_cache, v_cache, block_pairs)
     n = block_pairs.shape[0] if block_pairs.numel() else 0
     if n:
         _need(block_pairs.dtype == torch.int64 and block_pairs.is_cuda and block_pairs.is_contiguous()
@@ -133,6 +169,7 @@ def pa_prefill(out, q, k_cache, v_cache, cu_q, q_start, block_tables, scale, num
           and block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] >= S,
           "cu_q [S+1], q_start [S], block_tables [S, M] must be int32")
     _need(block_tables.is_contiguous(), "block_tables must be contiguous")
+    _on_current_device(out, q, cu_q, q_start, block_tables, status)
     L.check(_LIB.pa_prefill(out.data_ptr(), dtype_code(out.dtype), q.data_ptr(), T, cu_q.data_ptr(),
                             q_start.data_ptr(), S, int(max_q_len), H, k_cache.data_ptr(), v_cache.data_ptr(),
                             NB, bs, Hkv, D, dtype_code(k_cache.dtype), block_tables.data_ptr(),
@@ -154,6 +191,7 @@ def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens
     Gn = prefix_len.numel()
     _need(group_start.dtype == torch.int32 and prefix_len.dtype == torch.int32 and group_start.numel() == Gn + 1,
           "group_start [G+1] and prefix_len [G] must be int32")
+    _on_current_device(out, q, block_tables, context_lens, group_start, prefix_len, workspace, status)
     need = _LIB.pa_decode_shared_prefix_workspace_size(B, H, Hkv, Gn, int(max_group_size), int(max_prefix_len))
     if need == 0:
         raise PAError(L.PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix_workspace_size")
@@ -210,6 +248,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_k
           and block_tables.is_contiguous(), "block_tables must be contiguous int32 [B, max_blocks]")
     _need(context_lens.dtype == torch.int32 and context_lens.numel() == B, "context_lens must be int32 [B]")
     _need(workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace must be a CUDA uint8 tensor")
+    _on_current_device(out, q, block_tables, context_lens, workspace)
     L.check(_LIB.pa_decode(out.data_ptr(), dtype_code(out.dtype), q.data_ptr(), B, H,
                            k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
                            dtype_code(k_cache.dtype), block_tables.data_ptr(), block_tables.shape[1],
@@ -232,6 +271,7 @@ def pa_decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, sca
     _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B
           and block_tables.is_contiguous(), "block_tables must be contiguous int32 [B, max_blocks]")
     _need(context_lens.dtype == torch.int32 and context_lens.numel() == B, "context_lens must be int32 [B]")
+    _on_current_device(out, q, block_tables, context_lens)
     L.check(_LIB.pa_decode_no_alloc(out.data_ptr(), dtype_code(out.dtype), q.data_ptr(), B, H,
                                     k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
                                     dtype_code(k_cache.dtype), block_tables.data_ptr(),
@@ -239,6 +279,14 @@ def pa_decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, sca
                                     int(max_context_len), float(scale), int(partition_tokens),
                                     _stream(stream)),
             "pa_decode_no_alloc")
+
+
+def pa_decode_no_alloc_error(stream=None) -> int:
+    """Synchronise, return and clear the device status word of the last
+    pa_decode_no_alloc call on the current device."""
+    st = C.c_int32(0)
+    L.check(_LIB.pa_decode_no_alloc_error(_stream(stream), C.byref(st)), "pa_decode_no_alloc_error")
+    return st.value
 
 
 def pa_workspace_init(workspace, stream=None) -> None:

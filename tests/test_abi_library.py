@@ -106,3 +106,13 @@ def test_plain_c_program_uses_the_host_calls(lib, tmp_path):
     assert build.returncode == 0, build.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stderr)
+
+
+def test_checked_calls_need_a_status_word(lib):
+    from paged_kv_cache_142_gb300 import _lib as L
+    # the checked append and copy require their status word (before any launch)
+    assert lib.pa_reshape_and_cache_checked(None, None, 3, None, None, None, 8, 16, 2, 128, 1, None,
+                                            None) == L.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks_checked(None, None, 8, 16, 2, 128, 1, None, 2, None, None) == L.PA_ERR_INVALID_ARG
+    # the no-alloc status read needs somewhere to put it
+    assert lib.pa_decode_no_alloc_error(None, None) == L.PA_ERR_INVALID_ARG

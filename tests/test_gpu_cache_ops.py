@@ -138,3 +138,122 @@ def test_layered_argument_errors(ops):
     assert lib.pa_copy_blocks_layers(16, 16, 16 * 2 * 16 * 64 + 1, 2, 16, 16, 2, 64, 1, 16, 1,
                                      None) == L.PA_ERR_INVALID_ARG
     assert lib.pa_copy_blocks_layers(16, 16, 0, 0, 16, 16, 2, 64, 1, 16, 1, None) == L.PA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# checked mode: a device status word instead of silent skips
+# ---------------------------------------------------------------------------
+def _oracle_raises(fn, *args) -> bool:
+    try:
+        fn(*args)
+    except ValueError:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("bad", [False, True])
+def test_checked_append_reports_slots_past_the_pool(ops, dtype, bad):
+    """The oracle raises on a slot past the pool; the checked append reports
+    it in the status word, writes no such slot, and writes every other token
+    bit-exactly (padding skipped)."""
+    NB, Hkv, bs, D, T = 6, 2, 8, 64, 9
+    rng = np.random.default_rng(5 + bad)
+    key = W.Values.from_f32(rng.standard_normal((T, Hkv, D)).astype(np.float32), dtype)
+    val = W.Values.from_f32(rng.standard_normal((T, Hkv, D)).astype(np.float32), dtype)
+    slots = np.array([5, -1, 17, 47, 0, -3, 40, 9, 33], dtype=np.int64)
+    if bad:
+        slots[[2, 6]] = [NB * bs, NB * bs + 11]
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    kc = torch.zeros((NB, Hkv, bs, D), dtype=dt, device="cuda")
+    vc = torch.zeros_like(kc)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.pa_reshape_and_cache(to_device(key), to_device(val), torch.from_numpy(slots).cuda(), kc, vc,
+                             status=status)
+    kb, vb = raw_bits(key.bits), raw_bits(val.bits)
+    ek = np.zeros((NB, Hkv, bs, D), dtype=kb.dtype)
+    ev = np.zeros_like(ek)
+    raised = _oracle_raises(oracle.reshape_and_cache, kb, vb, ek.copy(), ev.copy(), slots)
+    assert int(status.item()) == (1 if raised else 0)
+    assert raised == bad
+    keep = slots < NB * bs
+    oracle.reshape_and_cache(kb[keep], vb[keep], ek, ev, slots[keep])
+    assert np.array_equal(cache_bits(kc), ek)
+    assert np.array_equal(cache_bits(vc), ev)
+
+
+def _invalid_pair_sets(NB, rng):
+    perm = rng.permutation(NB)
+    good = np.stack([perm[:12], perm[12:24]], axis=1).astype(np.int64)
+    out = {}
+    dup = good.copy()
+    dup[7, 1] = dup[2, 1]                 # one destination named twice
+    out["duplicate destination"] = dup
+    src = good.copy()
+    src[4, 1] = src[9, 0]                 # a destination that is another pair's source
+    out["destination is a source"] = src
+    self_ = good.copy()
+    self_[0, 1] = self_[0, 0]             # a block copied onto itself
+    out["self copy"] = self_
+    rng_ = good.copy()
+    rng_[11, 0] = NB                      # a source outside the pool
+    out["source outside the pool"] = rng_
+    neg = good.copy()
+    neg[3, 1] = -1                        # a destination outside the pool
+    out["negative destination"] = neg
+    return good, out
+
+
+@pytest.mark.parametrize("dtype,bs,Hkv,D", [("bf16", 16, 8, 128), ("f32", 8, 2, 64)])
+def test_checked_copy_validates_before_copying(ops, dtype, bs, Hkv, D):
+    """Valid pairs: status stays 0 and the copy is bit-exact.  Each invalid
+    set (the oracle raises ValueError before copying anything): status 1 and
+    no block changes."""
+    NB = 48
+    rng = np.random.default_rng(21)
+    k = W.Values.from_f32(rng.standard_normal((NB, Hkv, bs, D)).astype(np.float32), dtype)
+    v = W.Values.from_f32(rng.standard_normal((NB, Hkv, bs, D)).astype(np.float32), dtype)
+    good, bad_sets = _invalid_pair_sets(NB, rng)
+    for name, pairs in [("valid", good)] + list(bad_sets.items()):
+        kc = to_device(k).contiguous()
+        vc = to_device(v).contiguous()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ops.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).cuda(), status=status)
+        ek, ev = raw_bits(k.bits).copy(), raw_bits(v.bits).copy()
+        raised = _oracle_raises(oracle.copy_blocks, ek, ev, pairs)
+        assert raised == (name != "valid"), name
+        assert int(status.item()) == (1 if raised else 0), name
+        assert np.array_equal(cache_bits(kc), ek), name   # unchanged when the oracle raised
+        assert np.array_equal(cache_bits(vc), ev), name
+
+
+def test_checked_copy_many_pairs_and_sticky_status(ops):
+    """Several hundred pairs (the validation spans several tiles of pairs):
+    a duplicate between the first and the last tile is found; a status left
+    non-zero suppresses a later checked copy; empty pair lists do nothing."""
+    NB, Hkv, bs, D = 1400, 2, 8, 64
+    rng = np.random.default_rng(8)
+    kc = torch.randn((NB, Hkv, bs, D), device="cuda")
+    vc = torch.randn((NB, Hkv, bs, D), device="cuda")
+    perm = rng.permutation(NB)
+    n = 650
+    pairs = np.stack([perm[:n], perm[n:2 * n]], axis=1).astype(np.int64)
+    k0, v0 = kc.clone(), vc.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).cuda(), status=status)
+    assert int(status.item()) == 0
+    ek, ev = k0.cpu().numpy(), v0.cpu().numpy()
+    oracle.copy_blocks(ek, ev, pairs)
+    assert np.array_equal(kc.cpu().numpy(), ek) and np.array_equal(vc.cpu().numpy(), ev)
+    bad = pairs.copy()
+    bad[n - 1, 1] = bad[1, 1]
+    k1, v1 = kc.clone(), vc.clone()
+    ops.pa_copy_blocks(kc, vc, torch.from_numpy(bad).cuda(), status=status)
+    assert int(status.item()) == 1
+    assert torch.equal(kc, k1) and torch.equal(vc, v1)
+    # the status is still 1: a valid checked copy is suppressed too
+    ops.pa_copy_blocks(kc, vc, torch.from_numpy(pairs[:5].copy()).cuda(), status=status)
+    assert int(status.item()) == 1 and torch.equal(kc, k1)
+    status.zero_()
+    ops.pa_copy_blocks(kc, vc, torch.empty((0, 2), dtype=torch.int64, device="cuda"), status=status)
+    assert int(status.item()) == 0 and torch.equal(kc, k1)
