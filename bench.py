@@ -184,69 +184,130 @@ def _oracle_sample_setup(wl, nseq):
     return tables, kc, vc
 
 
+_POOL_STATE = None
+
+
+def _decode_share(args):
+    """Worker of the oracle pool: decode the given sequences in turn."""
+    import oracle
+    seqs = args
+    wl, tables, kc, vc, per_seq = _POOL_STATE
+    t0 = time.perf_counter()
+    for i in seqs:
+        oracle.paged_decode(wl.q.f32, kc, vc, tables, wl.context_lens, wl.scale, wl.num_kv_heads, seqs=[i])
+    return time.perf_counter() - t0, sum(per_seq[i] for i in seqs)
+
+
 def _oracle_child(argv):
-    """Runs in a child process with one BLAS thread: time the oracle decoding
-    sequences 0..nseq-1 in turn, either ``steps`` decodes or for ``budget`` s."""
-    budget, nseq, steps = float(argv[0]), int(argv[1]), int(argv[2])
+    """Runs in a child process with no CUDA in it, one BLAS thread per
+    process.  Phase "seq": one process decodes the first 64 sequences in turn,
+    for ``budget`` s.  Phase "batch": ``procs`` forked processes decode all
+    nseq sequences per step, each a disjoint share, for ``steps`` steps or
+    until ``budget`` s have passed (per-step wall times).  Mode "both" runs
+    the two phases on one set-up."""
+    mode, budget, nseq, steps, procs = argv[0], float(argv[1]), int(argv[2]), int(argv[3]), int(argv[4])
     import oracle
     wl = W.gqa_bf16()
     tables, kc, vc = _oracle_sample_setup(wl, nseq)
     e = W.elem_bytes(wl.dtype)
     per_seq = [step_bytes(wl.context_lens[i:i + 1], 1, wl.num_q_heads, wl.num_kv_heads,
                           wl.head_dim, e, e)[0] for i in range(nseq)]
-    times, nbytes = [], []
-    t_start = time.perf_counter()
-    k = 0
-    while True:
-        i = k % nseq
-        t0 = time.perf_counter()
-        oracle.paged_decode(wl.q.f32, kc, vc, tables, wl.context_lens, wl.scale, wl.num_kv_heads,
-                            seqs=[i])
-        times.append(time.perf_counter() - t0)
-        nbytes.append(per_seq[i])
-        k += 1
-        if (steps and k >= steps) or (not steps and time.perf_counter() - t_start >= budget):
-            break
-    print(json.dumps({"times": times, "bytes": nbytes}))
+    out = {}
+    if mode in ("seq", "both"):
+        times, nbytes = [], []
+        t_start = time.perf_counter()
+        k = 0
+        while True:
+            i = k % min(nseq, 64)
+            t0 = time.perf_counter()
+            oracle.paged_decode(wl.q.f32, kc, vc, tables, wl.context_lens, wl.scale, wl.num_kv_heads,
+                                seqs=[i])
+            times.append(time.perf_counter() - t0)
+            nbytes.append(per_seq[i])
+            k += 1
+            if time.perf_counter() - t_start >= budget:
+                break
+        out.update(times=times, bytes=nbytes)
+    if mode in ("batch", "both"):
+        import multiprocessing as mp
+        global _POOL_STATE
+        _POOL_STATE = (wl, tables, kc, vc, per_seq)    # shared with the workers by fork
+        # longest first over the shares, so every process gets a similar load
+        order = sorted(range(nseq), key=lambda i: -int(wl.context_lens[i]))
+        shares = [order[r::procs] for r in range(procs)]
+        step_times, step_bytes_ = [], []
+        with mp.get_context("fork").Pool(procs) as pool:   # this process never touches CUDA
+            pool.map(_decode_share, [[0]] * procs)          # workers up
+            t_start = time.perf_counter()
+            while True:
+                t0 = time.perf_counter()
+                res = pool.map(_decode_share, shares)
+                step_times.append(time.perf_counter() - t0)
+                step_bytes_.append(sum(r[1] for r in res))
+                if (steps and len(step_times) >= steps) or (not steps and time.perf_counter() - t_start >= budget):
+                    break
+        out.update(procs=procs, step_times=step_times, step_bytes=step_bytes_, seqs_per_step=nseq)
+    print(json.dumps(out))
 
 
-def run_oracle(budget_s: float, nseq: int, steps: int = 0):
+def run_oracle(mode: str, budget_s: float, nseq: int, steps: int = 0, procs: int = 1):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle_child",
-                        str(budget_s), str(nseq), str(steps)],
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle_child", mode,
+                        str(budget_s), str(nseq), str(steps), str(procs)],
                        capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError(f"oracle baseline failed:\n{r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def cpu_baseline(budget_s: float) -> dict:
+    """The fp64 oracle on the host: all cores (one process per core, one BLAS
+    thread each, decoding the whole 256-sequence batch per step) and a single
+    core (the first 64 sequences in turn), each for about ``budget_s`` s."""
+    cores = os.cpu_count() or 1
+    res = run_oracle("both" if cores > 1 else "seq", budget_s, 256, procs=cores)
+    t1 = sum(res["times"])
+    single = {"value": round(sum(res["bytes"]) / t1 / 1e9, 4), "unit": UNIT, "cores": 1,
+              "seq_steps_per_s": round(len(res["times"]) / t1, 2),
+              "sample": (f"fp64 oracle decode of the first 64 of the 256 sequences in turn for {t1:.1f} s "
+                         f"({len(res['times'])} sequence decodes), 1 process, 1 BLAS thread")}
+    if cores == 1:
+        return dict(single, kind="oracle", single_core=dict(single))
+    wall = sum(res["step_times"])
+    n = len(res["step_times"])
+    return {"value": round(sum(res["step_bytes"]) / wall / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "seq_steps_per_s": round(256 * n / wall, 2),
+            "sample": (f"fp64 oracle decode of all 256 sequences per step, {n} steps in {wall:.1f} s, "
+                       f"{cores} processes (one per host core, 1 BLAS thread each) on disjoint shares"),
+            "single_core": single}
+
+
 def reference_arm(args):
-    """The oracle as the reference arm: each step decodes a bounded sample of
-    the workload's sequences, sized so the K + W steps take about two minutes."""
+    """The oracle as the reference arm, on all the host's cores: each step
+    decodes the whole 256-sequence batch, split over one process per core;
+    W warm-up steps, then K timed steps."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cal = run_oracle(0, 4, steps=4)
-    t_seq = max(1e-4, sum(cal["times"]) / len(cal["times"]))
-    per_step = max(1, min(256, int(120.0 / max(1, args.steps + args.warmup) / t_seq)))
-    res = run_oracle(0, per_step, steps=per_step * (args.steps + args.warmup))
-    times = res["times"][per_step * args.warmup:]
-    nbytes = res["bytes"][per_step * args.warmup:]
+    cores = os.cpu_count() or 1
+    res = run_oracle("batch", 0, 256, steps=args.steps + args.warmup, procs=cores)
+    times = res["step_times"][args.warmup:]
+    nbytes = res["step_bytes"][args.warmup:]
     t = sum(times)
     value = sum(nbytes) / t / 1e9
-    sample = (f"fp64 oracle decode of {per_step} of the 256 sequences per step "
-              f"(single process, 1 BLAS thread)")
+    sample = (f"fp64 oracle decode of all 256 sequences per step, {cores} processes (one per host core, "
+              f"1 BLAS thread each) on disjoint shares")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * t / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "num_seqs": 256, "sample_seqs_per_step": per_step},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "config": {"workload": WORKLOAD, "num_seqs": 256},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
-        "seq_steps_per_s": round(per_step * args.steps / t, 3),
+        "seq_steps_per_s": round(256 * args.steps / t, 3),
     }
     print(json.dumps(line), flush=True)
 
@@ -348,42 +409,20 @@ def measure_extras(ops, dev, seed: int = 1420) -> dict:
     # shared-prefix decode: the beam-search workload's last step, 64 sequences
     # = one 3000-token prompt + 32 tokens of their own (the prompt's 187 full
     # blocks shared by all), plain decode against one group of 64
-    Sb, pref, own = 64, 3000, 32
-    NBs = pref // bs + 1 + Sb * (own // bs + 2)
-    al = ops.BlockAllocator(NBs, bs)
-    root = al.seq_create()
-    al.append_tokens(root, pref)
-    beams = [al.fork(root) for _ in range(Sb)]
-    al.free_seq(root)
-    for _ in range(own):
-        al.append_slots(beams)
-    tb, ln = al.export_tables(beams, (pref + own) // bs + 2)
-    al.close()
-    ksp = torch.randn((NBs, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
-    vsp = torch.randn((NBs, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
-    qs = torch.randn((Sb, Hq_, D), generator=g, device=dev).to(torch.bfloat16)
-    osp = torch.empty((Sb, Hq_, D), dtype=torch.bfloat16, device=dev)
-    t_tb, t_ln = torch.from_numpy(tb).to(dev), torch.from_numpy(ln).to(dev)
-    mlen = int(ln.max())
+    sp = _shared_prefix_case(ops, dev, g, Hq_, Hkv, D, bs)
+    Sb, pref, own, shared = sp["Sb"], sp["pref"], sp["own"], sp["shared"]
+    osp, qs, ksp, vsp, t_tb, t_ln, mlen = sp["out"], sp["q"], sp["k"], sp["v"], sp["tables"], sp["lens"], sp["mlen"]
+    gs, pl_, st_sp, tb, ln = sp["group_start"], sp["prefix_len"], sp["status"], sp["tables_np"], sp["lens_np"]
     wsd = ops.make_workspace(Sb, Hq_, Hkv, D, bs, "bf16", mlen, device=dev)
-    gs = torch.tensor([0, Sb], dtype=torch.int32, device=dev)
-    shared = (pref // bs) * bs
-    pl_ = torch.tensor([shared], dtype=torch.int32, device=dev)
-    st_sp = torch.zeros(1, dtype=torch.int32, device=dev)
-    wss = ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D), Hkv, mlen, gs, pl_, Sb,
-                                      shared, status=st_sp)
+    wss = sp["launch"]()
     t_plain = _event_time_us(lambda: ops.pa_decode(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D), Hkv, mlen,
                                                    wsd), 50, stream)
-    t_shared = _graph_time_us(lambda: ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D),
-                                                                  Hkv, mlen, gs, pl_, Sb, shared, workspace=wss,
-                                                                  status=st_sp))
-    t_shared_e = _event_time_us(lambda: ops.pa_decode_shared_prefix(osp, qs, ksp, vsp, t_tb, t_ln, 1.0 / math.sqrt(D),
-                                                                    Hkv, mlen, gs, pl_, Sb, shared, workspace=wss,
-                                                                    status=st_sp), 50, stream)
+    t_shared = _graph_time_us(lambda: sp["launch"](wss))
+    t_shared_e = _event_time_us(lambda: sp["launch"](wss), 50, stream)
     logical = int(ln.sum()) * Hkv * D * 2 * 2 + 2 * Sb * Hq_ * D * 2
     unique_blocks = len(set(tb[:, :int(ln.max()) // bs + 1].ravel().tolist()))
     sp_ok = int(st_sp.item()) == 0
-    del ksp, vsp
+    del ksp, vsp, sp, osp, qs
     # decode on the other decode configurations: MHA (G = 1) and long-context
     # split-K (G = 8, block 16 and 32).  Lengths, pool and free list are the
     # workloads'; the values are drawn on the device (throughput only; parity
@@ -489,6 +528,101 @@ def _prefill_case(ops, dev, g, S_, n_=2048, Hq_=32, Hkv=8, D=128, bs=16):
         ops.pa_prefill(op, qp, kpp, vpp, cu, st0, tab, 1.0 / math.sqrt(D), Hkv, n_, status=stat)
 
     return launch, S_ * 2.0 * D * Hq_ * n_ * (n_ + 1), stat
+
+
+def _shared_prefix_case(ops, dev, g, Hq_=32, Hkv=8, D=128, bs=16):
+    """The beam-search workload's last step for the shared-prefix decode: 64
+    sequences = one 3000-token prompt + 32 tokens of their own, built with the
+    allocator (fork, then one append per step), values drawn on the device.
+    ``launch(workspace=None)`` runs pa_decode_shared_prefix on one group of 64
+    and returns its workspace."""
+    import torch
+    Sb, pref, own = 64, 3000, 32
+    NBs = pref // bs + 1 + Sb * (own // bs + 2)
+    al = ops.BlockAllocator(NBs, bs)
+    root = al.seq_create()
+    al.append_tokens(root, pref)
+    beams = [al.fork(root) for _ in range(Sb)]
+    al.free_seq(root)
+    for _ in range(own):
+        al.append_slots(beams)
+    tb, ln = al.export_tables(beams, (pref + own) // bs + 2)
+    al.close()
+    c = {"Sb": Sb, "pref": pref, "own": own, "shared": (pref // bs) * bs, "tables_np": tb, "lens_np": ln}
+    c["k"] = torch.randn((NBs, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    c["v"] = torch.randn((NBs, Hkv, bs, D), generator=g, device=dev).to(torch.bfloat16)
+    c["q"] = torch.randn((Sb, Hq_, D), generator=g, device=dev).to(torch.bfloat16)
+    c["out"] = torch.empty((Sb, Hq_, D), dtype=torch.bfloat16, device=dev)
+    c["tables"], c["lens"] = torch.from_numpy(tb).to(dev), torch.from_numpy(ln).to(dev)
+    c["mlen"] = int(ln.max())
+    c["group_start"] = torch.tensor([0, Sb], dtype=torch.int32, device=dev)
+    c["prefix_len"] = torch.tensor([c["shared"]], dtype=torch.int32, device=dev)
+    c["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch(workspace=None):
+        return ops.pa_decode_shared_prefix(c["out"], c["q"], c["k"], c["v"], c["tables"], c["lens"],
+                                           1.0 / math.sqrt(D), Hkv, c["mlen"], c["group_start"],
+                                           c["prefix_len"], Sb, c["shared"], workspace=workspace,
+                                           status=c["status"])
+
+    c["launch"] = launch
+    return c
+
+
+def kernel_profile(args):
+    """Profiling case for the per-kernel DRAM captures: --warmup untimed, then
+    --steps launches of each of, in this order, the step's append (256
+    tokens into the batch-256 pool), the 32-layer append, the 64-pair copy
+    (one layer and 32 layers), the shared-prefix decode (its pass and its
+    merge) and the 16 x 2048 causal prefill."""
+    import torch
+    dev = torch.device("cuda", 0)
+    from paged_kv_cache_142_gb300 import build as B_
+    B_.build(quiet=True)
+    from paged_kv_cache_142_gb300 import ops
+    g = torch.Generator(device=dev).manual_seed(7)
+    wl = W.gqa_bf16(values=False)
+    Hkv, D, bs, T = wl.num_kv_heads, wl.head_dim, wl.block_size, wl.num_seqs
+    kc = torch.zeros((wl.num_blocks, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    key = torch.randn((T, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    val = torch.randn((T, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.randperm(wl.num_blocks * bs, generator=g, device=dev)[:T].to(torch.int64)
+    Lyr, NBl, npairs = 32, 512, 64
+    kl = torch.zeros((Lyr, NBl, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vl = torch.zeros_like(kl)
+    keyl = torch.randn((Lyr, T, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    vall = torch.randn((Lyr, T, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    slotsl = torch.randperm(NBl * bs, generator=g, device=dev)[:T].to(torch.int64)
+    perm = torch.randperm(NBl, generator=g, device=dev)
+    pairs = torch.stack([perm[:npairs], perm[npairs:2 * npairs]], dim=1).to(torch.int64).contiguous()
+    sp = _shared_prefix_case(ops, dev, g, 32, Hkv, D, bs)
+    wss = sp["launch"]()
+    pf_launch, _, pf_stat = _prefill_case(ops, dev, g, 16)
+    cases = [
+        ("append", lambda: ops.pa_reshape_and_cache(key, val, slots, kc, vc)),
+        ("append_layers", lambda: ops.pa_reshape_and_cache_layers(keyl, vall, slotsl, kl, vl)),
+        ("copy", lambda: ops.pa_copy_blocks(kl[0], vl[0], pairs)),
+        ("copy_layers", lambda: ops.pa_copy_blocks_layers(kl, vl, pairs)),
+        ("shared_prefix", lambda: sp["launch"](wss)),
+        ("prefill", pf_launch),
+    ]
+    times = {}
+    for name, fn in cases:
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        times[name] = round(a.elapsed_time(b) * 1000.0 / args.steps, 2)
+    if int(sp["status"].item()) != 0 or int(pf_stat.item()) != 0:
+        raise RuntimeError("a profiled kernel reported an error")
+    print(json.dumps({"profile_kernels": True, "us_per_call": times,
+                      "shared_prefix_unique_blocks": int(len(set(sp["tables_np"].ravel().tolist())))}), flush=True)
 
 
 def prefill_profile(args):
@@ -790,13 +924,7 @@ def gpu_arm(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        res = run_oracle(args.cpu_seconds, 64)
-        tot = sum(res["times"])
-        cpu = {"value": round(sum(res["bytes"]) / tot / 1e9, 4), "unit": UNIT, "cores": 1,
-               "kind": "oracle",
-               "sample": (f"fp64 oracle decode of the first 64 of the 256 sequences in turn for "
-                          f"{tot:.1f} s ({len(res['times'])} sequence decodes, "
-                          f"{len(res['times']) / tot:.1f} seq-steps/s), 1 process, 1 BLAS thread")}
+        cpu = cpu_baseline(args.cpu_seconds)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -856,13 +984,18 @@ def main():
                     help="split-K partition size passed to pa_decode (0 = automatic)")
     ap.add_argument("--profile", action="store_true",
                     help="device-resident steps only (no e2e leg, no CPU baseline)")
+    ap.add_argument("--profile-kernels", action="store_true",
+                    help="profiling case: --warmup + --steps launches of each secondary kernel "
+                         "(append, copy, shared-prefix decode, prefill) at its bench size")
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="PROMPTS",
                     help="profiling case: only pa_prefill on PROMPTS causal prompts of 2048 tokens "
                          "(32 q / 8 kv heads), --warmup + --steps launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.profile_prefill:
+    if args.profile_kernels:
+        kernel_profile(args)
+    elif args.profile_prefill:
         prefill_profile(args)
     elif args.impl == "reference":
         reference_arm(args)

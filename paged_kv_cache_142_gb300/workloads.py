@@ -207,12 +207,12 @@ def gqa_lens(rng: np.random.Generator, num_seqs: int, median: float = 800.0,
 
 
 def gqa_bf16(seed: int = SEEDS["gqa_bf16"], num_seqs: int = 256,
-             block_size: int = 16) -> DecodeWorkload:
+             block_size: int = 16, values: bool = True) -> DecodeWorkload:
     rng = np.random.Generator(np.random.PCG64(seed))
     lens = gqa_lens(rng, num_seqs)
     NB = _pool_for(lens, block_size, 1.2)
     return _make("gqa_bf16", DTYPE_BF16, lens, 32, 8, 128, block_size, NB, 0.5, seed, rng,
-                 extra={"len_dist": "lognormal(median 800, sigma 0.5) clipped [16,4096]"})
+                 extra={"len_dist": "lognormal(median 800, sigma 0.5) clipped [16,4096]"}, values=values)
 
 
 def long_bf16(seed: int = SEEDS["long_bf16"], block_size: int = 16, num_seqs: int = 8,
