@@ -15,9 +15,11 @@ Prints one JSON line (rank 0):
              K,V go host->device in one copy, the kernels run (a CUDA graph
              per buffer set), the output comes back; the upload of the next
              step and the download of the last overlap the kernels
-  roofline   pa_decode's algorithmic bytes / its mean CUDA-event duration,
-             against the measured HBM copy bandwidth; DRAM traffic from the
-             committed ncu summary while the kernel source is unchanged
+  roofline   pa_decode's algorithmic bytes / its mean duration (CUDA events
+             around back-to-back launches on the launching stream), against
+             the measured HBM copy bandwidth; DRAM traffic from the committed
+             ncu summary of the full-size launch while the kernel source is
+             unchanged
   cpu_baseline  the fp64 oracle on a bounded sample, on the host
   extras     the other rows' kernels on their own workloads: multi-layer
              append and copy, paged prefill, shared-prefix decode, the MHA
@@ -740,10 +742,24 @@ def gpu_arm(args):
     if world > 1:
         dist.barrier()
     total_ms = t0e.elapsed_time(t1e)
+    # The decode kernel's own average duration: K2 back-to-back launches on
+    # the launching stream between one event pair (the kernel's launches
+    # follow one another as they do inside the steps).  For comparison, the
+    # same decode with an event pair around each launch after an append,
+    # which also counts each launch's start-up gap.
     K2 = min(K, 500)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
     w0b = time.time()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
     for k in range(K2):
+        ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws,
+                      partition_tokens=args.partition_tokens)
+    d1.record(stream)
+    torch.cuda.synchronize(dev)
+    dec_ms = [d0.elapsed_time(d1) / K2]
+    K3 = min(K, 100)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K3)]
+    for k in range(K3):
         ops.pa_reshape_and_cache(new_k, new_v, t_slots, kc, vc)
         ev[k][0].record(stream)
         ops.pa_decode(out, q, kc, vc, t_tables, t_lens, wl.scale, Hkv, e2e_max_len, ws,
@@ -751,7 +767,7 @@ def gpu_arm(args):
         ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     sampler.mark(w0b, time.time())
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_pair_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     dev_status = ops.pa_workspace_error(ws)
     if dev_status != 0:
         raise RuntimeError(f"device status {dev_status} after the timed steps")
@@ -941,6 +957,7 @@ def gpu_arm(args):
                                   if world > 1 else "single GPU"},
         "seq_steps_per_s": round(sum_seqs / (t_step * 1e-3), 1),
         "decode_ms": round(t_dec, 5),
+        "decode_ms_event_pair_per_launch": round(dec_pair_ms, 5),
         "decode_bytes_per_step": decode_bytes,
         "append_bytes_per_step": append_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,

@@ -171,17 +171,27 @@ __device__ __forceinline__ int tail_class(int len, int pt) {
 
 // Builds lens, prefix_full and tail_seq and returns the number of sequences
 // with a last partition; every thread calls it; the CTA is synchronised on
-// return.  hist: kTailBuckets + 1 ints of scratch.  CTA 0 reports lengths
+// return.  scratch: (nthreads / 32 + 1) * kTailBuckets + 1 ints of shared
+// memory that no role touches before the set-up ends.  CTA 0 reports lengths
 // outside [0, max_context_len] in the workspace error word.
+//
+// The tail order is a stable counting sort spread over every warp: thread t
+// takes a run of `per` consecutive sequences, so warp w covers a contiguous
+// range; each warp counts its range's sequences per class, one warp turns the
+// counts into each (warp, class) pair's first position (classes longest
+// first, warps in sequence order within a class), and each warp then places
+// its own range, 32 sequences per round.
 __device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* lens,
                                                 int32_t* prefix_full, int32_t* tail_seq,
-                                                int* warp_sums, int* hist, int tid, int nthreads) {
+                                                int* warp_sums, int* scratch, int tid, int nthreads) {
   const int nseq = p.num_seqs, pt = p.part_tokens, hkv = p.num_kv_heads;
-  const int lane = tid & 31, warp = tid >> 5;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  int* cnt = scratch;                              // [warp][class]: counts, then first positions
+  int* n_tail_word = scratch + nwarps * kTailBuckets;
   const int per = (nseq + nthreads - 1) / nthreads;
   const int beg = min(nseq, tid * per);
   const int end = min(nseq, beg + per);
-  if (tid < kTailBuckets) hist[tid] = 0;
+  for (int i = tid; i < nwarps * kTailBuckets; i += nthreads) cnt[i] = 0;
   __syncthreads();
   int lf = 0;
   for (int i = beg; i < end; ++i) {
@@ -191,7 +201,7 @@ __device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* 
     lens[i] = len;
     lf += (len / pt) * hkv;
     const int c = tail_class(len, pt);
-    if (c >= 0) atomicAdd(&hist[c], 1);
+    if (c >= 0) atomicAdd(&cnt[warp * kTailBuckets + c], 1);
   }
   int xf = lf;
 #pragma unroll
@@ -208,42 +218,55 @@ __device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* 
     rf += (lens[i] / pt) * hkv;
   }
   if (tid == nthreads - 1) prefix_full[nseq] = rf;
-  __syncthreads();
   if (warp == 0) {
-    // class bases, longest class first: lane l owns classes 63 - 2l and 62 - 2l
+    // class totals and bases, longest class first: lane l owns classes
+    // 63 - 2l and 62 - 2l; then each warp's first position per class
     static_assert(kTailBuckets == 64, "two classes per lane");
-    const int c0 = hist[kTailBuckets - 1 - 2 * lane], c1 = hist[kTailBuckets - 2 - 2 * lane];
-    int x = c0 + c1;
+    const int ca = kTailBuckets - 1 - 2 * lane, cb = ca - 1;
+    int ta = 0, tb = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      ta += cnt[w * kTailBuckets + ca];
+      tb += cnt[w * kTailBuckets + cb];
+    }
+    int x = ta + tb;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, off);
       if (lane >= off) x += y;
     }
     const int total = __shfl_sync(0xffffffffu, x, 31);
-    const int ex = x - c0 - c1;
-    __syncwarp();
-    hist[kTailBuckets - 1 - 2 * lane] = ex;
-    hist[kTailBuckets - 2 - 2 * lane] = ex + c0;
-    __syncwarp();
-    // stable placement, 32 sequences at a time
-    for (int c = 0; c < nseq; c += 32) {
-      const int s = c + lane;
-      const int k = s < nseq ? tail_class(lens[s], pt) : -1;
-      const unsigned m = __match_any_sync(0xffffffffu, k);
-      const int rank = __popc(m & ((1u << lane) - 1u));
-      const int pos = k >= 0 ? hist[k] + rank : 0;
-      __syncwarp();
-      if (k >= 0) {
-        tail_seq[pos] = s;
-        if (rank == 0) hist[k] += __popc(m);
-      }
-      __syncwarp();
+    int ra = x - ta - tb, rb = ra + ta;
+    for (int w = 0; w < nwarps; ++w) {
+      const int na = cnt[w * kTailBuckets + ca], nb = cnt[w * kTailBuckets + cb];
+      cnt[w * kTailBuckets + ca] = ra;
+      cnt[w * kTailBuckets + cb] = rb;
+      ra += na;
+      rb += nb;
     }
-    if (lane == 0) hist[kTailBuckets] = total;
+    if (lane == 0) *n_tail_word = total;
   }
   __syncthreads();
-  const int n_tail = hist[kTailBuckets];
-  __syncthreads();  // hist is shared scratch of later roles
+  // stable placement of this warp's range, 32 sequences per round
+  const int wbeg = min(nseq, warp * 32 * per), wend = min(nseq, (warp + 1) * 32 * per);
+  int* wcnt = cnt + warp * kTailBuckets;
+  for (int c = wbeg; c < wend; c += 32) {
+    const int s = c + lane;
+    const int k = s < wend ? tail_class(lens[s], pt) : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, k);
+    const int rank = __popc(m & ((1u << lane) - 1u));
+    const int pos = k >= 0 ? wcnt[k] + rank : 0;
+    __syncwarp();
+    if (k >= 0) {
+      tail_seq[pos] = s;
+      if (rank == 0) wcnt[k] += __popc(m);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  const int n_tail = *n_tail_word;
+  // the scratch is later overwritten by tensor copies (the async proxy)
+  ptx::fence_proxy_async_smem();
+  __syncthreads();  // the scratch belongs to later roles from here on
   return n_tail;
 }
 
@@ -420,42 +443,21 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   const int hkv = p.num_kv_heads;
   const int bs = p.block_size;
 
-  if (tid == 0) {
-    for (int s = 0; s < NSK; ++s) {
-      ptx::mbar_init(&bars[kKFull + s], 1);
-      ptx::mbar_init(&bars[kKFull + kUmmaMaxStages + s], 1);
-      ptx::mbar_init(&bars[kKEmpty + s], 1);
+  // barriers: one per thread, each initialiser fencing its own inits
+  if (tid < kUmmaBarriers) {
+    uint32_t count = 1;
+    if (tid >= kGroup0 && tid < kGroup0 + 2 * kUmmaGroupBars) {
+      const int gi = (tid - kGroup0) % kUmmaGroupBars;
+      if ((gi >= kSEmpty && gi < kSEmpty + 2) || (gi >= kPFull && gi < kPFull + 2) ||
+          (gi >= kOEmpty && gi < kOEmpty + 2))
+        count = 4;  // one arrival per compute warp
+    } else if (tid >= kItemEmpty && tid < kItemEmpty + 2 * kUmmaQueue) {
+      count = kUmmaQueueReaders;
     }
-    for (int s = 0; s < NSV; ++s) {
-      ptx::mbar_init(&bars[kVFull + s], 1);
-      ptx::mbar_init(&bars[kVFull + kUmmaMaxStages + s], 1);
-      ptx::mbar_init(&bars[kVEmpty + s], 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      uint64_t* gb = bars + kGroup0 + g * kUmmaGroupBars;
-      ptx::mbar_init(&gb[kQFull], 1);   // one query slot per group
-      ptx::mbar_init(&gb[kQEmpty], 1);
-      for (int b = 0; b < 2; ++b) {
-        ptx::mbar_init(&gb[kSFull + b], 1);
-        ptx::mbar_init(&gb[kSEmpty + b], 4);
-        ptx::mbar_init(&gb[kPFull + b], 4);
-        ptx::mbar_init(&gb[kPEmpty + b], 1);
-        ptx::mbar_init(&gb[kOFull + b], 1);
-        ptx::mbar_init(&gb[kOEmpty + b], 4);
-      }
-    }
-    for (int g = 0; g < 2; ++g) {
-      ptx::mbar_init(&bars[kDrainQK + g], 1);
-      ptx::mbar_init(&bars[kDrainPV + g], 1);
-    }
-    for (int q = 0; q < 2 * kUmmaQueue; ++q) {
-      ptx::mbar_init(&bars[kItemFull + q], 1);
-      ptx::mbar_init(&bars[kItemEmpty + q], kUmmaQueueReaders);
-    }
-    ptx::mbar_init(&bars[kNever], 1);
-    for (int i = 0; i < 6; ++i) flags[i] = 0;
+    ptx::mbar_init(&bars[tid], count);
     ptx::mbar_init_fence();
   }
+  if (tid < 6) flags[tid] = 0;
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, TMEM_COLS);
     ptx::tc_fence_before();
@@ -463,8 +465,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   // launched behind the step's append with programmatic serialisation, the
   // set-up above overlaps it; every input is read after this point
   ptx::griddep_wait();
+  // the K ring is idle until the set-up ends: it holds the sort's scratch
   const int n_tail = build_item_order(p, lens, prefix_full, tail_seq, warp_sums,
-                                      reinterpret_cast<int*>(small), tid, kUmmaThreads);  // syncs
+                                      reinterpret_cast<int*>(kring), tid, kUmmaThreads);  // syncs
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_full = prefix_full[p.num_seqs];
@@ -504,7 +507,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const int box_rows = min(bs, kUmmaTile);
     const int bs_log = __ffs(bs) - 1;  // block size is a power of two
     // warp 0 claims items for both groups and publishes them; warp 10 reads.
-    // A claim is made only when the stream takes a group's last tile of its
+    // Each group's first item is fixed by the CTA index (items blockIdx.x and
+    // gridDim.x + blockIdx.x: the first 2 * gridDim.x items, the longest, need
+    // no claim at the start of the launch); later ones are claimed from the
+    // shared counter, only when the stream takes a group's last tile of its
     // current item, so no CTA holds work another could start sooner.
     auto publish_item = [&](int g, uint32_t k) -> int {
       int w = -1;
@@ -512,7 +518,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         const int slot = g * kUmmaQueue + static_cast<int>(k % kUmmaQueue);
         wait(&bars[kItemEmpty + slot], ((k / kUmmaQueue) & 1u) ^ 1u, aborted, stop);
         if (!aborted) {
-          w = atomicAdd(item_counter, 1);
+          w = k == 0 ? g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)
+                     : atomicAdd(item_counter, 1) + 2 * static_cast<int>(gridDim.x);
           if (w >= ctx.total) w = -1;
         }
         queue[slot] = w;
@@ -536,7 +543,19 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       if (r.j == 0) {
         const int nb = ((r.it.t0 + r.it.ntok + bs - 1) >> bs_log) - b0;
         const int32_t* trow = p.block_tables + static_cast<int64_t>(r.it.seq) * p.max_blocks_per_seq + b0;
-        for (int j = lane; j < nb; j += 32) gtbl[j] = trow[j];
+        for (int j0 = 0; j0 < nb; j0 += 128) {  // four loads in flight per lane, then the stores
+          int v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u + lane;
+            v[u] = j < nb ? __ldg(trow + j) : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u + lane;
+            if (j < nb) gtbl[j] = v[u];
+          }
+        }
         __syncwarp();
         if (!is_v && lane == 0) {
           uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
