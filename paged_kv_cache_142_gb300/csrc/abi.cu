@@ -465,6 +465,12 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
   pa_status st = prepare_kernel(fn, kPrefillThreads, smem, &ctas);
   if (st != PA_OK) return st;
   if (ctas > items) ctas = static_cast<int>(items);
+  if (p.mode == 0) {
+    // blocks of pairs holding about two waves of the launch's items
+    const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+    int64_t pb = (2 * static_cast<int64_t>(ctas) + p.tiles_per_seq - 1) / (p.tiles_per_seq > 0 ? p.tiles_per_seq : 1);
+    p.pair_block = static_cast<int32_t>(pb < 1 ? 1 : (pb > pairs ? pairs : pb));
+  }
   CUtensorMap tmq, tmk, tmv;
   const uint32_t box_rows = static_cast<uint32_t>(p.block_size < 128 ? p.block_size : 128);
   if (!encode_q_tokens(&tmq, q, static_cast<uint64_t>(p.num_tokens),

@@ -23,7 +23,9 @@
 // runs while P.V of tile t is in flight.
 //
 // One CTA per SM, 288 threads, persistent over (tile of TQ tokens, sequence,
-// kv head) items, later (longer) tiles first:
+// kv head) items, in blocks of a few (sequence, kv head) pairs so that the
+// CTAs at work share those pairs' keys and values in L2, later (longer) tiles
+// first within a block:
 //  * warp 0 loads the item's query rows (2-D TMA boxes, one per head and
 //    64-dim half; two buffers, so the next item's rows load during this
 //    item) and its K tiles (one 4-D TMA box per block, as in decode)
@@ -97,8 +99,8 @@ __device__ __forceinline__ void bad_input(const PrefillParams& p) {
   if (p.status) atomicExch(p.status, kDevErrInvalidArg);
 }
 
-// Work item w.  Mode 0 (prefill): (tile of TQ tokens, sequence, kv head),
-// later tiles first, causal keys [0, position].  Mode 1 (shared prefix):
+// Work item w.  Mode 0 (prefill): (tile of TQ tokens, sequence, kv head) in
+// blocks of pairs, later tiles first within a block, causal keys [0, position].  Mode 1 (shared prefix):
 // (prefix partition, tile of TQ members, group, kv head) over the group's
 // prefix keys, read through its first member's table.  Mode 2 (own tokens):
 // (member, kv head) over keys [prefix, len) of the member's table.  Mode 3:
@@ -117,11 +119,20 @@ __device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, It
     if (mode == 2) w -= n1;
   }
   if (mode == 0) {
-    const int per_tile = p.num_seqs * hkv;
-    const int tile = p.tiles_per_seq - 1 - w / per_tile;
-    const int rem = w - (w / per_tile) * per_tile;
-    it.seq = rem / hkv;
-    it.kvh = rem - it.seq * hkv;
+    // blocks of pair_block (sequence, kv head) pairs, one block after the
+    // other; within a block later tiles first, pairs fastest.  The CTAs
+    // working at the same time then share a few pairs' keys and values, which
+    // stay in L2 between their tiles.
+    const int T = p.tiles_per_seq;
+    const int npairs = p.num_seqs * hkv;
+    const int per_block = p.pair_block * T;
+    const int blk = w / per_block;
+    const int r = w - blk * per_block;
+    const int nb = min(p.pair_block, npairs - blk * p.pair_block);  // pairs in this block
+    const int tile = T - 1 - r / nb;
+    const int pair = blk * p.pair_block + (r - (r / nb) * nb);
+    it.seq = pair / hkv;
+    it.kvh = pair - it.seq * hkv;
     it.qb = p.cu_q[it.seq];
     const int n = p.cu_q[it.seq + 1] - it.qb;
     it.tok0 = tile * TQ;
