@@ -368,7 +368,7 @@ __device__ __forceinline__ void wait(uint64_t* bar, uint32_t parity, bool& abort
                                      volatile int* stop, uint64_t limit_ns = kWaitLimitNs) {
   if (aborted || ptx::mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = ptx::global_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  while (!ptx::mbar_try_wait_sleep(bar, parity, ptx::kSleepHintNs)) {
     if (*stop || ptx::global_ns() - t0 > limit_ns) {
       aborted = true;
       *stop = 1;
