@@ -466,9 +466,16 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
   if (st != PA_OK) return st;
   if (ctas > items) ctas = static_cast<int>(items);
   if (p.mode == 0) {
-    // blocks of pairs holding about two waves of the launch's items
+    // While every (sequence, kv head) pair's keys and values fit in half of L2
+    // (the other half for the query and output streams), one block holds all
+    // pairs: the tile-major order, whose round-robin waves have the most even
+    // costs.  Past that, blocks of about two waves of the launch's items, so
+    // that the CTAs at work share a few pairs' keys in L2.
     const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+    const int64_t tokens = static_cast<int64_t>(p.tiles_per_seq) * (128 / G);  // longest chunk, rounded up
+    const int64_t kv_bytes = pairs * tokens * 2 * 128 * 2;                       // K and V, bf16, head_dim 128
     int64_t pb = (2 * static_cast<int64_t>(ctas) + p.tiles_per_seq - 1) / (p.tiles_per_seq > 0 ? p.tiles_per_seq : 1);
+    if (kv_bytes <= (int64_t(64) << 20)) pb = pairs;
     p.pair_block = static_cast<int32_t>(pb < 1 ? 1 : (pb > pairs ? pairs : pb));
   }
   CUtensorMap tmq, tmk, tmv;
