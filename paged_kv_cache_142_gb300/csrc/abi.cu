@@ -78,12 +78,14 @@ pa_status check_cache_shape(int32_t num_blocks, int32_t block_size, int32_t num_
 constexpr int kUmmaThreadsHost = 448;
 constexpr int kUmmaTileBytesHost = 32768;
 // per compute group scratch of the tensor-core decode (with an item's totals for G >= 8)
-constexpr int umma_small_bytes_host(int G) { return G >= 8 ? 1280 : 1024; }
+// (must match umma_small_bytes in decode_umma.cuh)
+constexpr int umma_small_bytes_host(int HG, int kh) { return (HG >= 8 || kh == 2) ? 1280 : 1024; }
 constexpr int kPrefillThreads = 288;  // must match the prefill kernel
 
 struct Plan {
   DecodeKernelInfo info;
   bool umma;       // tensor-core kernel (bf16, head_dim 128, block >= 8)
+  int kh;          // kv heads per work item (tensor cores: 2 for G <= 4, blocks of 8..64)
   int stages, stages_v;
   int tbl_stride;
   int off_q, off_p, off_small, off_lens;
@@ -110,12 +112,18 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   // bf16 K/V with head_dim 128 and blocks of >= 8 tokens run on the tensor
   // cores; everything else on the CUDA-core kernel
   pl->umma = dtype == PA_DTYPE_BF16 && head_dim == 128 && block_size >= 8 &&
-             pa::decode_umma_fn(G) != nullptr;
+             pa::decode_umma_fn(G, 1) != nullptr;
+  // two kv heads per item: one TMA box per block covers both heads (twice the
+  // bytes per copy) and half as many items, with the same MMA shapes
+  pl->kh = pl->umma && G <= 4 && num_kv_heads % 2 == 0 && block_size <= 64 &&
+                   pa::decode_umma_fn(G, 2) != nullptr
+               ? 2
+               : 1;
   if (!pl->umma && !pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
     return PA_ERR_UNSUPPORTED;
   // partition size: a multiple of the block size and of the stage (tensor
   // cores: of the 128-token tile); at most part/2 partitions per sequence
-  const int64_t unit = pl->umma ? 128 : pl->info.tokens_per_stage;
+  const int64_t unit = pl->umma ? 128 / pl->kh : pl->info.tokens_per_stage;
   const int64_t gran = block_size > unit ? block_size : unit;
   // tensor cores: long partitions (each item costs a block-table load, a
   // query load and an epilogue; fewer items mean fewer merges), 4096 tokens
@@ -124,7 +132,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   int64_t def_pt = kDefaultPartTokens;
   if (pl->umma) {
     def_pt = max_context_len > 4096 ? 4096 : 2048;
-    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    const int64_t units = static_cast<int64_t>(num_seqs) * (num_kv_heads / pl->kh);
     const int64_t sms = pa::device_sm_count();
     while (def_pt > 256 && units * ceil_div(max_context_len, def_pt) < 2 * sms) def_pt /= 2;
   }
@@ -138,9 +146,10 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     // K ring | V ring | queries [2 groups] | P [2 groups][2] | per-group
     // scratch | barriers, flags | table slices [2 streams][2 groups] |
     // lengths | prefix | align slack
-    const int64_t pbytes = G <= 8 ? 4096 : 8192;
+    const int HG = G * pl->kh;  // query heads per item
+    const int64_t pbytes = HG <= 8 ? 4096 : 8192;
     const int64_t tbl_stride = round_up(pt / block_size + 1, 4);
-    const int64_t fixed = 2 * 4096 + 2 * 2 * pbytes + 2 * umma_small_bytes_host(G) + 256 + 1024 + 4 * tbl_stride * 4 +
+    const int64_t fixed = 2 * 4096 + 2 * 2 * pbytes + 2 * umma_small_bytes_host(HG, pl->kh) + 256 + 1024 + 4 * tbl_stride * 4 +
                           round_up(static_cast<int64_t>(num_seqs) * 4, 16) +
                           2 * round_up((static_cast<int64_t>(num_seqs) + 4) / 4 * 4 * 4, 16) + 1024;
     int sk = 3, sv = 3;
@@ -159,7 +168,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
       pl->off_p = static_cast<int>(off);
       off += 2 * 2 * pbytes;
       pl->off_small = static_cast<int>(off);
-      off += 2 * umma_small_bytes_host(G) + 256;  // per-group scratch, then the two item queues
+      off += 2 * umma_small_bytes_host(HG, pl->kh) + 256;  // per-group scratch, then the two item queues
       pl->off_bar = static_cast<int>(off);
       off += 1024;
       pl->off_tbl = static_cast<int>(off);  // [K/V stream][group]
@@ -171,6 +180,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
       pl->smem = static_cast<int>(off + 1024);  // slack to align the base to 1024 bytes
     }
   }
+  if (!pl->umma) pl->kh = 1;
   if (!pl->umma && !pl->info.fn &&
       !pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
     return PA_ERR_UNSUPPORTED;
@@ -189,15 +199,17 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     if (off + 64 > kMaxSmem) return PA_ERR_UNSUPPORTED;  // + static shared memory
     pl->smem = static_cast<int>(off);
   }
-  // workspace: header | counters | (max, sum) partials | output partials
-  const int64_t rows = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  // workspace: header | counters | (max, sum) partials | output partials, by
+  // (sequence, kv-head group) row and the group's kh * G query heads
+  const int64_t rows = static_cast<int64_t>(num_seqs) * (num_kv_heads / pl->kh);
+  const int64_t heads = static_cast<int64_t>(G) * pl->kh;
   pl->ws_counters = 256;
   int64_t w = 256 + round_up(rows * 4, 256);
   pl->ws_ml = static_cast<size_t>(w);
   if (pl->max_parts > 1) {
-    w += round_up(rows * pl->max_parts * G * 2 * 4, 256);
+    w += round_up(rows * pl->max_parts * heads * 2 * 4, 256);
     pl->ws_o = static_cast<size_t>(w);
-    w += round_up(rows * pl->max_parts * G * static_cast<int64_t>(head_dim) * 4, 256);
+    w += round_up(rows * pl->max_parts * heads * static_cast<int64_t>(head_dim) * 4, 256);
   } else {
     pl->ws_o = static_cast<size_t>(w);
   }
@@ -205,7 +217,7 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   return PA_OK;
 }
 
-const void* plan_kernel(const Plan& pl) { return pl.umma ? pa::decode_umma_fn(pl.group) : pl.info.fn; }
+const void* plan_kernel(const Plan& pl) { return pl.umma ? pa::decode_umma_fn(pl.group, pl.kh) : pl.info.fn; }
 int plan_threads(const Plan& pl) { return pl.umma ? kUmmaThreadsHost : pa::kDecodeThreads; }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -689,7 +701,7 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
   int ctas = 0;
   st = prepare_kernel(plan_kernel(pl), plan_threads(pl), pl.smem, &ctas);
   if (st != PA_OK) return st;
-  const int64_t max_items = static_cast<int64_t>(num_seqs) * num_kv_heads * pl.max_parts;
+  const int64_t max_items = static_cast<int64_t>(num_seqs) * (num_kv_heads / pl.kh) * pl.max_parts;
   if (ctas > max_items) ctas = static_cast<int>(max_items);
 
   DecodeParams p;
@@ -739,10 +751,13 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
     const int64_t q_rows = static_cast<int64_t>(num_seqs) * num_q_heads;
     if (cache_rows >= (int64_t(1) << 31) || q_rows >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
     CUtensorMap tmk, tmv, tmq;
-    const uint32_t box_rows = static_cast<uint32_t>(block_size < 128 ? block_size : 128);
+    // a box: one block's tokens of the item's kv heads (two heads: a whole
+    // block of both, contiguous in the pool), at most 128 rows
+    const uint32_t box_rows = static_cast<uint32_t>(
+        pl.kh == 2 ? 2 * block_size : (block_size < 128 ? block_size : 128));
     if (!encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
         !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
-        !encode_rows_128(&tmq, q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(pl.group)))
+        !encode_rows_128(&tmq, q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(pl.group * pl.kh)))
       return PA_ERR_CUDA;
     void* args[] = {&p, &tmk, &tmv, &tmq};
     // programmatic serialisation: the kernel's set-up may overlap the tail of

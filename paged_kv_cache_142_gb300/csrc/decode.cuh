@@ -73,8 +73,9 @@ struct DecodeKernelInfo {
 // Returns false if the combination is not compiled.
 bool decode_kernel_info(int dtype_bf16, int head_dim, int group, DecodeKernelInfo* info);
 
-// Tensor-core kernel (bf16, head_dim 128) for a GQA group, or nullptr.
-const void* decode_umma_fn(int group);
+// Tensor-core kernel (bf16, head_dim 128) for a GQA group with 1 or 2 kv
+// heads per work item, or nullptr.
+const void* decode_umma_fn(int group, int kv_per_item);
 
 // Paged prefill (tensor cores, bf16, head_dim 128, block size >= 8).
 struct PrefillParams {

@@ -71,8 +71,13 @@ constexpr int kUmmaTile = 128;           // tokens per tile (MMA M)
 constexpr int kUmmaTileBytes = 32768;    // one K or V tile: 16 row groups x 2 halves x 8 rows x 128 B
 constexpr int kUmmaMaxStages = 8;
 constexpr int kUmmaQBytes = 4096;        // query tile: 2 halves x 16 rows x 128 B (one per group)
-// per group: reductions and rescale factors (G <= 4), plus an item's totals (G >= 8)
-__host__ __device__ constexpr int umma_small_bytes(int G) { return G >= 8 ? 1280 : 1024; }
+// per compute group: maxima and rescale factors [2][4][16] + [2][16] floats,
+// then the row-sum scratch: [4][16] while an item's totals stay in registers
+// (one kv head per item, G <= 4), or [2][4][16] + the final maxima [2][16]
+// when they go through shared memory (HG = KH * G query heads per item)
+__host__ __device__ constexpr int umma_small_bytes(int HG, int KH) {
+  return (HG >= 8 || KH == 2) ? 1280 : 1024;
+}
 constexpr int kUmmaGroupBars = 16;
 constexpr int kUmmaQueue = 8;            // per-group item queue depth
 constexpr int kUmmaQueueReaders = 9;     // V stream, 2 Q.K and 2 P.V warps, a group's 4 compute warps
@@ -103,8 +108,10 @@ constexpr int kItemFull = kDrainPV + 2;                   // [group][kUmmaQueue]
 constexpr int kItemEmpty = kItemFull + 2 * kUmmaQueue;    // [group][kUmmaQueue]
 constexpr int kNever = kItemEmpty + 2 * kUmmaQueue;       // no role ever arrives (timeout-path test)
 
+// An item: partition `part` of sequence `seq` for kv-head group `kvg` (kv
+// heads kvg * KH .. kvg * KH + KH - 1, KH = 1 or 2 per item).
 struct Item {
-  int seq, kvh, part, len, t0, ntok, nparts;
+  int seq, kvg, part, len, t0, ntok, nparts;
 };
 
 // Item enumeration: first every full partition (part_tokens tokens) of
@@ -124,6 +131,8 @@ struct Ctx {
   const int32_t* tail_seq;     // sequences with a last partition, in item order
   const int32_t* lens;
   int n_full, total;
+  int nkg;                     // kv-head groups per sequence (num_kv_heads / KH)
+  int tile_tokens;             // tokens per 128-row tile (128 / KH)
 };
 
 // First s with prefix[s + 1] > w (prefix non-decreasing, prefix[0] = 0).
@@ -139,18 +148,18 @@ __device__ __forceinline__ int seq_of(int w, const int32_t* prefix, int nseq) {
 
 __device__ __forceinline__ Item item_at(const Ctx& c, int w) {
   Item it;
-  const int hkv = c.p->num_kv_heads;
+  const int nkg = c.nkg;
   const int pt = c.p->part_tokens;
   if (w < c.n_full) {
     it.seq = seq_of(w, c.prefix_full, c.p->num_seqs);
     const int u = w - c.prefix_full[it.seq];
-    it.part = u / hkv;
-    it.kvh = u - it.part * hkv;
+    it.part = u / nkg;
+    it.kvg = u - it.part * nkg;
   } else {
     const int v = w - c.n_full;
-    const int sp = v / hkv;
+    const int sp = v / nkg;
     it.seq = c.tail_seq[sp];
-    it.kvh = v - sp * hkv;
+    it.kvg = v - sp * nkg;
     it.part = c.lens[it.seq] / pt;
   }
   it.len = c.lens[it.seq];
@@ -183,8 +192,9 @@ __device__ __forceinline__ int tail_class(int len, int pt) {
 // its own range, 32 sequences per round.
 __device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* lens,
                                                 int32_t* prefix_full, int32_t* tail_seq,
-                                                int* warp_sums, int* scratch, int tid, int nthreads) {
-  const int nseq = p.num_seqs, pt = p.part_tokens, hkv = p.num_kv_heads;
+                                                int* warp_sums, int* scratch, int tid, int nthreads,
+                                                int nkg) {
+  const int nseq = p.num_seqs, pt = p.part_tokens;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
   int* cnt = scratch;                              // [warp][class]: counts, then first positions
   int* n_tail_word = scratch + nwarps * kTailBuckets;
@@ -199,7 +209,7 @@ __device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* 
     if (blockIdx.x == 0 && (raw < 0 || raw > p.max_context_len)) atomicExch(p.ws_err, kDevErrInvalidArg);
     const int len = decode_detail::clamp_len(raw, p.max_context_len);
     lens[i] = len;
-    lf += (len / pt) * hkv;
+    lf += (len / pt) * nkg;
     const int c = tail_class(len, pt);
     if (c >= 0) atomicAdd(&cnt[warp * kTailBuckets + c], 1);
   }
@@ -215,7 +225,7 @@ __device__ __forceinline__ int build_item_order(const DecodeParams& p, int32_t* 
   for (int w = 0; w < warp; ++w) rf += warp_sums[w];
   for (int i = beg; i < end; ++i) {
     prefix_full[i] = rf;
-    rf += (lens[i] / pt) * hkv;
+    rf += (lens[i] / pt) * nkg;
   }
   if (tid == nthreads - 1) prefix_full[nseq] = rf;
   if (warp == 0) {
@@ -283,7 +293,7 @@ struct GroupIter {
 struct Rec {
   int g;          // compute group
   Item it;
-  int j, nt, nv;  // tile index in the item, tiles of the item, valid rows
+  int j, nt, nv;  // tile index in the item, tiles of the item, valid tokens
   uint32_t u;     // tile index in the CTA's stream (stage u % depth of each ring)
   uint32_t ug;    // tile index within the group (S/P/O buffers)
   uint32_t qi;    // item index within the group (query slot phase)
@@ -299,7 +309,7 @@ __device__ __forceinline__ void seek(const Ctx& c, GroupIter& s, int g, NextW&& 
     if (w < 0) break;
     s.it = item_at(c, w);
     if (s.it.ntok > 0) {
-      s.nt = (s.it.ntok + kUmmaTile - 1) / kUmmaTile;
+      s.nt = (s.it.ntok + c.tile_tokens - 1) / c.tile_tokens;
       s.j = 0;
       s.valid = true;
       return;
@@ -331,7 +341,7 @@ struct Stream {
     r.it = s.it;
     r.j = s.j;
     r.nt = s.nt;
-    r.nv = min(kUmmaTile, s.it.ntok - s.j * kUmmaTile);
+    r.nv = min(c.tile_tokens, s.it.ntok - s.j * c.tile_tokens);
     r.u = u++;
     r.ug = ug++;
     r.qi = s.items;
@@ -398,7 +408,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 }  // namespace umma_detail
 
-template <int G>
+// KH kv heads per item (1, or 2 for G <= 4 and blocks of 8..64 tokens): a
+// tile then holds 128 / KH tokens of each of the item's kv heads, its rows
+// block by block and, within a block, kv head by kv head, as one block's K
+// (or V) of consecutive kv heads lies in the pool; one TMA box per block
+// covers both heads.  Q.K^T puts all KH x G heads against every row (row r
+// keeps the G columns of its own kv head); P is block-diagonal (row r has
+// non-zero columns only for its kv head's G heads), so P.V gives every head
+// its own output.  Both products keep their shapes (N = 16).
+template <int G, int KH>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
     paged_decode_umma_kernel(const __grid_constant__ DecodeParams p,
                              const __grid_constant__ CUtensorMap tm_k,
@@ -406,12 +424,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                              const __grid_constant__ CUtensorMap tm_q) {
   using namespace umma_detail;
   static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
+  static_assert(KH == 1 || (KH == 2 && G <= 4), "kv heads per item");
   constexpr int HD = 128;
-  constexpr int NP = G <= 8 ? 16 : 32;     // P.V columns: hi heads, then lo heads
+  constexpr int HG = KH * G;               // query heads of an item
+  constexpr int TT = kUmmaTile / KH;       // tokens per tile
+  constexpr int NP = HG <= 8 ? 16 : 32;    // P.V columns: hi heads, then lo heads
   constexpr int LO = NP / 2;               // column of the lo half
   constexpr int PGRP = NP / 8;             // 8-column core matrices per P row group
-  constexpr int PB = umma_p_bytes(G);      // one P buffer
-  constexpr uint32_t TMEM_COLS = G <= 8 ? 128 : 256;  // S[2][2] x 16, then O[2][2] x NP
+  constexpr int PB = umma_p_bytes(HG);     // one P buffer
+  constexpr uint32_t TMEM_COLS = HG <= 8 ? 128 : 256;  // S[2][2] x 16, then O[2][2] x NP
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -434,7 +455,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   int32_t* lens = reinterpret_cast<int32_t*>(smem + p.off_lens);
   int32_t* prefix_full = reinterpret_cast<int32_t*>(smem + p.off_prefix);
   int32_t* tail_seq = prefix_full + ((p.num_seqs + 4) & ~3);
-  constexpr int kSmall = umma_small_bytes(G);
+  constexpr int kSmall = umma_small_bytes(HG, KH);
   volatile int* queue = reinterpret_cast<volatile int*>(small + 2 * kSmall);  // [group][kUmmaQueue]
 
   const int tid = threadIdx.x;
@@ -442,6 +463,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   const int lane = tid & 31;
   const int hkv = p.num_kv_heads;
   const int bs = p.block_size;
+  const int bs_log_c = __ffs(bs) - 1;  // block size is a power of two
 
   // barriers: one per thread, each initialiser fencing its own inits
   if (tid < kUmmaBarriers) {
@@ -466,12 +488,13 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   // set-up above overlaps it; every input is read after this point
   ptx::griddep_wait();
   // the K ring is idle until the set-up ends: it holds the sort's scratch
+  const int nkg = hkv / KH;
   const int n_tail = build_item_order(p, lens, prefix_full, tail_seq, warp_sums,
-                                      reinterpret_cast<int*>(kring), tid, kUmmaThreads);  // syncs
+                                      reinterpret_cast<int*>(kring), tid, kUmmaThreads, nkg);  // syncs
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_full = prefix_full[p.num_seqs];
-  const Ctx ctx{&p, prefix_full, tail_seq, lens, n_full, n_full + n_tail * p.num_kv_heads};
+  const Ctx ctx{&p, prefix_full, tail_seq, lens, n_full, n_full + n_tail * nkg, nkg, TT};
   bool aborted = false;
   int* item_counter = p.ws_err + 1;   // next unclaimed item (all CTAs)
   int* done_counter = p.ws_err + 2;   // CTAs finished
@@ -504,7 +527,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     uint64_t* full = bars + (is_v ? kVFull : kKFull);
     uint64_t* empty = bars + (is_v ? kVEmpty : kKEmpty);
     const int NS = is_v ? NSV : NSK;
-    const int box_rows = min(bs, kUmmaTile);
+    // a box: box_tok tokens of each of the item's KH kv heads (KH = 2: one
+    // whole block of both heads)
+    const int box_tok = KH == 1 ? min(bs, kUmmaTile) : bs;
+    const int box_rows = KH * box_tok;
     const int bs_log = __ffs(bs) - 1;  // block size is a power of two
     // warp 0 claims items for both groups and publishes them; warp 10 reads.
     // Each group's first item is fixed by the CTA index (items blockIdx.x and
@@ -561,10 +587,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           uint64_t* gb = bars + kGroup0 + r.g * kUmmaGroupBars;
           wait(&gb[kQEmpty], (r.qi & 1u) ^ 1u, aborted, stop);
           if (!aborted) {
-            ptx::mbar_arrive_expect_tx(&gb[kQFull], 2u * G * 128u);
+            ptx::mbar_arrive_expect_tx(&gb[kQFull], 2u * HG * 128u);
             unsigned char* qd = qbuf + r.g * kUmmaQBytes;
             for (int h = 0; h < 2; ++h)
-              ptx::tma_load_2d(qd + h * 2048, &tm_q, 64 * h, r.it.seq * p.num_q_heads + r.it.kvh * G,
+              ptx::tma_load_2d(qd + h * 2048, &tm_q, 64 * h, r.it.seq * p.num_q_heads + r.it.kvg * HG,
                                &gb[kQFull], pol_q);
             if (r.g) qfill1 = r.qi + 1;
             else qfill0 = r.qi + 1;
@@ -572,18 +598,18 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
       }
       // this lane's block of the tile (lanes < nbox)
-      const int tok0 = r.it.t0 + r.j * kUmmaTile;
-      const int nbox = (r.nv + box_rows - 1) / box_rows;
+      const int tok0 = r.it.t0 + r.j * TT;
+      const int nbox = (r.nv + box_tok - 1) / box_tok;
       int row = 0;
       if (lane < nbox) {
-        const int tok = tok0 + lane * box_rows;
+        const int tok = tok0 + lane * box_tok;
         const int lb = tok >> bs_log;
         int phys = gtbl[lb - b0];
         if (phys < 0 || phys >= p.num_blocks) {  // never read outside the pool
           atomicExch(p.ws_err, kDevErrInvalidArg);
           phys = 0;
         }
-        row = ((phys * hkv + r.it.kvh) << bs_log) + (tok - (lb << bs_log));
+        row = ((phys * hkv + r.it.kvg * KH) << bs_log) + (tok - (lb << bs_log));
       }
       uint64_t* fb = &full[(wrap & 1u) * kUmmaMaxStages + slot];
       if (lane == 0) {
@@ -706,15 +732,35 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       }
       aborted = __shfl_sync(0xffffffffu, aborted, 0);
       if (aborted) break;
-      const int nks = (r.nv + 15) / 16;
-      if (r.nv & 15) {
-        const int row0 = r.nv, nrows = nks * 16 - r.nv;   // 1..15 rows, both halves
-        for (int c = lane; c < nrows * 16; c += 32) {
-          const int rr = row0 + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
-          *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
-              make_uint4(0, 0, 0, 0);
+      int nks;
+      if (KH == 1) {
+        // the valid rows are a prefix; zero the rest of its last 16-row step
+        nks = (r.nv + 15) / 16;
+        if (r.nv & 15) {
+          const int row0 = r.nv, nrows = nks * 16 - r.nv;   // 1..15 rows, both halves
+          for (int c = lane; c < nrows * 16; c += 32) {
+            const int rr = row0 + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+            *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          ptx::fence_proxy_async_smem();
         }
-        ptx::fence_proxy_async_smem();
+      } else {
+        // the valid rows are the blocks holding a valid token (2 * bs rows
+        // each, 16-row steps); in the last one, both heads' rows past the end
+        const int nbv = (r.nv + bs - 1) >> bs_log_c;
+        nks = (nbv * 2 * bs) / 16;
+        const int pv = r.nv - ((nbv - 1) << bs_log_c);      // valid tokens of the last block
+        if (pv < bs) {
+          const int gap = bs - pv, base = (nbv - 1) * 2 * bs + pv;
+          for (int c = lane; c < 2 * gap * 16; c += 32) {
+            const int idx = c >> 4, half = (c >> 3) & 1, ch = c & 7;
+            const int rr = base + (idx >= gap ? bs + idx - gap : idx);
+            *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          ptx::fence_proxy_async_smem();
+        }
       }
       __syncwarp();
       if (lane == 0) {
@@ -753,11 +799,20 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const float sl2 = p.scale_log2;
     uint64_t* gb = bars + kGroup0 + cg * kUmmaGroupBars;
     unsigned char* gp = pbuf + cg * 2 * PB;
+    // Row r's kv head within the item (KH = 2: rows go block by block, and
+    // within a block bs rows of the first head, then bs of the second) and
+    // its token within the tile.
+    const int kl = KH == 1 ? 0 : (r >> bs_log_c) & 1;
+    const int rtok = KH == 1 ? r : ((r >> (bs_log_c + 1)) << bs_log_c) + (r & (bs - 1));
+    // the two rows that publish each kv head's per-head values: row 0 (the
+    // first head) and row bs (the second)
+    const bool publisher = r == 0 || (KH == 2 && r == bs);
     // An item's totals (final max, row sums) are needed by its epilogue,
-    // which runs after the next tile's softmax.  G <= 4 keeps them in
-    // registers, one copy per tile parity; G >= 8 is short of registers
-    // (128 per thread at 448 threads) and keeps them in shared memory.
-    constexpr bool kTotalsInSmem = G >= 8;
+    // which runs after the next tile's softmax.  G <= 4 with one kv head per
+    // item keeps them in registers, one copy per tile parity; otherwise each
+    // thread holds only its kv head's values or is short of registers (128
+    // per thread at 448 threads), and they go through shared memory.
+    constexpr bool kTotalsInSmem = HG >= 8 || KH == 2;
     constexpr int NF = kTotalsInSmem ? 1 : G;
     float* red_m = reinterpret_cast<float*>(small + cg * kSmall);  // [2][4][16]
     float* alpha_s = red_m + 2 * 4 * 16;  // [2][16]
@@ -766,14 +821,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     volatile int* merge_flag = flags + 1 + cg;
     volatile int* gabort = flags + 3 + cg;
 
-    float m_run[G], l_thr[G], o_acc[G];
+    float m_run[G], l_thr[G], o_acc[HG];
     float m_fin0[NF], l_fin0[NF], m_fin1[NF], l_fin1[NF];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m_run[g] = -CUDART_INF_F;
       l_thr[g] = 0.f;
-      o_acc[g] = 0.f;
     }
+#pragma unroll
+    for (int h = 0; h < HG; ++h) o_acc[h] = 0.f;
 #pragma unroll
     for (int g = 0; g < NF; ++g) {
       m_fin0[g] = m_fin1[g] = -CUDART_INF_F;
@@ -782,9 +838,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     auto write_zeros = [&](int g_owner, const Item& it) {
       if (g_owner != cg) return;  // the owning group writes the zero output
-      const int64_t ob = (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * HD + r;
+      const int64_t ob = (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvg * HG) * HD + r;
 #pragma unroll
-      for (int g = 0; g < G; ++g) decode_detail::store_out(p.out, p.out_bf16, ob + g * HD, 0.f);
+      for (int h = 0; h < HG; ++h) decode_detail::store_out(p.out, p.out_bf16, ob + h * HD, 0.f);
     };
 
     auto softmax = [&](const Rec& t) {
@@ -799,43 +855,64 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       }
       wait(&gb[kSFull + b], ph, aborted, stop);
       ptx::tc_fence_after();
-      uint32_t sr[G];
-      ptx::TmemLd<G>::run(tmem + lane_base + (cg * 2 + b) * 16, sr);
+      uint32_t sr[HG];
+      ptx::TmemLd<HG>::run(tmem + lane_base + (cg * 2 + b) * 16, sr);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&gb[kSEmpty + b]);
-      const bool valid = r < t.nv;
+      const bool valid = rtok < t.nv;
       float s[G], mx[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        s[g] = valid ? __uint_as_float(sr[g]) * sl2 : -CUDART_INF_F;
+        const uint32_t v = KH == 1 ? sr[g] : (kl ? sr[(KH - 1) * G + g] : sr[g]);  // this row's head g
+        s[g] = valid ? __uint_as_float(v) * sl2 : -CUDART_INF_F;
         mx[g] = s[g];
       }
+      // max over the warp's rows of the same kv head (KH = 2, bs < 32: lane
+      // bit bs tells the two heads apart, so that step is skipped)
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
+      for (int off = 16; off > 0; off >>= 1) {
+        if (KH == 2 && off == bs) continue;
 #pragma unroll
         for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
-      if (lane == 0) {
+      }
+      if (KH == 1) {
+        if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) red_m[(b * 4 + cw) * 16 + g] = mx[g];
+          for (int g = 0; g < G; ++g) red_m[(b * 4 + cw) * 16 + g] = mx[g];
+        }
+      } else if (bs < 32) {
+        // lanes 0 and bs hold the warp's maxima of the two kv heads
+        if (lane == 0 || lane == bs) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) red_m[(b * 4 + cw) * 16 + kl * G + g] = mx[g];
+        }
+      } else if (lane == 0) {
+        // the whole warp is one kv head's rows: the other head gets -inf
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          red_m[(b * 4 + cw) * 16 + kl * G + g] = mx[g];
+          red_m[(b * 4 + cw) * 16 + (kl ^ 1) * G + g] = -CUDART_INF_F;
+        }
       }
       ptx::bar_sync(bar_id, 128);
       float pr[G], al[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float mt = red_m[(b * 4) * 16 + g];
+        const int hh = kl * G + g;
+        float mt = red_m[(b * 4) * 16 + hh];
 #pragma unroll
-        for (int k = 1; k < 4; ++k) mt = fmaxf(mt, red_m[(b * 4 + k) * 16 + g]);
+        for (int k = 1; k < 4; ++k) mt = fmaxf(mt, red_m[(b * 4 + k) * 16 + hh]);
         const float mn = fmaxf(m_run[g], mt);
         al[g] = fast_exp2(m_run[g] - mn);
         pr[g] = valid ? fast_exp2(s[g] - mn) : 0.f;
         l_thr[g] = l_thr[g] * al[g] + pr[g];
         m_run[g] = mn;
       }
-      if (ctid == 0) {
+      if (publisher) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) alpha_s[b * 16 + g] = al[g];
+        for (int g = 0; g < G; ++g) alpha_s[b * 16 + kl * G + g] = al[g];
       }
       if constexpr (!kTotalsInSmem) {
         if (last) {
@@ -861,8 +938,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const uint32_t hb = __float_as_uint(pr[g]) & 0xffff0000u;
-        pc[g] = hb >> 16;
-        pc[LO + g] = __float_as_uint(pr[g] - __uint_as_float(hb)) >> 16;
+        const uint32_t lb = __float_as_uint(pr[g] - __uint_as_float(hb)) >> 16;
+        if (KH == 1) {
+          pc[g] = hb >> 16;
+          pc[LO + g] = lb;
+        } else {
+          // block-diagonal: this row's kv head's columns only
+          pc[g] = kl ? 0u : hb >> 16;
+          pc[LO + g] = kl ? 0u : lb;
+          pc[(KH - 1) * G + g] = kl ? hb >> 16 : 0u;
+          pc[LO + (KH - 1) * G + g] = kl ? lb : 0u;
+        }
       }
       uint32_t wp[NP / 2];
 #pragma unroll
@@ -886,32 +972,42 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
           for (int g = 0; g < G; ++g) lw[g] = l_thr[g];
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
+          for (int off = 16; off > 0; off >>= 1) {
+            if (KH == 2 && off == bs) continue;  // sums over rows of the same kv head
 #pragma unroll
             for (int g = 0; g < G; ++g) lw[g] += __shfl_xor_sync(0xffffffffu, lw[g], off);
-          if (lane == 0) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) red_l[(b * 4 + cw) * 16 + g] = lw[g];
           }
-          if (ctid == 0) {
+          if (KH == 1 || bs < 32) {
+            if (lane == 0 || (KH == 2 && lane == bs)) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) red_mf[b * 16 + g] = m_run[g];
+              for (int g = 0; g < G; ++g) red_l[(b * 4 + cw) * 16 + kl * G + g] = lw[g];
+            }
+          } else if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              red_l[(b * 4 + cw) * 16 + kl * G + g] = lw[g];
+              red_l[(b * 4 + cw) * 16 + (kl ^ 1) * G + g] = 0.f;
+            }
+          }
+          if (publisher) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) red_mf[b * 16 + kl * G + g] = m_run[g];
           }
         }
       }
     };
 
     auto epilogue = [&](const Rec& t) {
-      float mf[G], L[G];
+      float mf[HG], L[HG];
       if constexpr (kTotalsInSmem) {
         // every warp's totals of this item, written in its last tile's softmax
         const int pb = static_cast<int>(t.ug & 1u);
         ptx::bar_sync(bar_id, 128);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          mf[g] = red_mf[pb * 16 + g];
-          L[g] = red_l[(pb * 4) * 16 + g] + red_l[(pb * 4 + 1) * 16 + g] + red_l[(pb * 4 + 2) * 16 + g] +
-                 red_l[(pb * 4 + 3) * 16 + g];
+        for (int h = 0; h < HG; ++h) {
+          mf[h] = red_mf[pb * 16 + h];
+          L[h] = red_l[(pb * 4) * 16 + h] + red_l[(pb * 4 + 1) * 16 + h] + red_l[(pb * 4 + 2) * 16 + h] +
+                 red_l[(pb * 4 + 3) * 16 + h];
         }
       } else {
         float lf[G];
@@ -932,21 +1028,21 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 #pragma unroll
         for (int g = 0; g < G; ++g) L[g] = red_l[g] + red_l[16 + g] + red_l[32 + g] + red_l[48 + g];
       }
-      const int64_t obase = (static_cast<int64_t>(t.it.seq) * p.num_q_heads + t.it.kvh * G) * HD + r;
+      const int64_t obase = (static_cast<int64_t>(t.it.seq) * p.num_q_heads + t.it.kvg * HG) * HD + r;
       if (t.it.nparts == 1) {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, o_acc[g] / L[g]);
+        for (int h = 0; h < HG; ++h)
+          decode_detail::store_out(p.out, p.out_bf16, obase + h * HD, o_acc[h] / L[h]);
         return;
       }
-      const int row = t.it.seq * hkv + t.it.kvh;
+      const int row = t.it.seq * nkg + t.it.kvg;
       const int64_t rec = static_cast<int64_t>(row) * p.max_parts + t.it.part;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        p.ws_o[(rec * G + g) * HD + r] = o_acc[g];
-        if (ctid == g) {
-          p.ws_ml[rec * G * 2 + 2 * g] = mf[g];
-          p.ws_ml[rec * G * 2 + 2 * g + 1] = L[g];
+      for (int h = 0; h < HG; ++h) {
+        p.ws_o[(rec * HG + h) * HD + r] = o_acc[h];
+        if (ctid == h) {
+          p.ws_ml[rec * HG * 2 + 2 * h] = mf[h];
+          p.ws_ml[rec * HG * 2 + 2 * h + 1] = L[h];
         }
       }
       // release: every writer orders its partial stores before the barrier;
@@ -961,34 +1057,34 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       }
       ptx::bar_sync(bar_id, 128);
       if (*merge_flag) {
-        // last partition of this (sequence, kv head) to finish: merge all
-        // heads at once so the partial loads are independent
-        const float* ml = p.ws_ml + static_cast<int64_t>(row) * p.max_parts * G * 2;
-        const float* os = p.ws_o + static_cast<int64_t>(row) * p.max_parts * G * HD + r;
+        // last partition of this (sequence, kv-head group) to finish: merge
+        // all heads at once so the partial loads are independent
+        const float* ml = p.ws_ml + static_cast<int64_t>(row) * p.max_parts * HG * 2;
+        const float* os = p.ws_o + static_cast<int64_t>(row) * p.max_parts * HG * HD + r;
         const int np = t.it.nparts;
-        float M[G], Ls[G], Os[G];
+        float M[HG], Ls[HG], Os[HG];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          M[g] = -CUDART_INF_F;
-          Ls[g] = 0.f;
-          Os[g] = 0.f;
+        for (int h = 0; h < HG; ++h) {
+          M[h] = -CUDART_INF_F;
+          Ls[h] = 0.f;
+          Os[h] = 0.f;
         }
 #pragma unroll 4
         for (int q = 0; q < np; ++q)
 #pragma unroll
-          for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], __ldcg(ml + q * G * 2 + 2 * g));
+          for (int h = 0; h < HG; ++h) M[h] = fmaxf(M[h], __ldcg(ml + q * HG * 2 + 2 * h));
 #pragma unroll 2
         for (int q = 0; q < np; ++q) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float2 mlq = __ldcg(reinterpret_cast<const float2*>(ml + q * G * 2 + 2 * g));
-            const float wq = exp2f(mlq.x - M[g]);
-            Ls[g] = fmaf(wq, mlq.y, Ls[g]);
-            Os[g] = fmaf(wq, __ldcg(os + (static_cast<int64_t>(q) * G + g) * HD), Os[g]);
+          for (int h = 0; h < HG; ++h) {
+            const float2 mlq = __ldcg(reinterpret_cast<const float2*>(ml + q * HG * 2 + 2 * h));
+            const float wq = exp2f(mlq.x - M[h]);
+            Ls[h] = fmaf(wq, mlq.y, Ls[h]);
+            Os[h] = fmaf(wq, __ldcg(os + (static_cast<int64_t>(q) * HG + h) * HD), Os[h]);
           }
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g) decode_detail::store_out(p.out, p.out_bf16, obase + g * HD, Os[g] / Ls[g]);
+        for (int h = 0; h < HG; ++h) decode_detail::store_out(p.out, p.out_bf16, obase + h * HD, Os[h] / Ls[h]);
         if (ctid == 0) p.ws_counters[row] = 0;
       }
     };
@@ -1004,9 +1100,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&gb[kOEmpty + b]);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float o = __uint_as_float(orr[g]) + __uint_as_float(orr[LO + g]);
-        o_acc[g] = t.j == 0 ? o : fmaf(o_acc[g], alpha_s[b * 16 + g], o);
+      for (int h = 0; h < HG; ++h) {
+        const float o = __uint_as_float(orr[h]) + __uint_as_float(orr[LO + h]);
+        o_acc[h] = t.j == 0 ? o : fmaf(o_acc[h], alpha_s[b * 16 + h], o);
       }
       if (t.j == t.nt - 1) epilogue(t);
     };
@@ -1026,7 +1122,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       t.it = gi.it;
       t.j = gi.j;
       t.nt = gi.nt;
-      t.nv = min(kUmmaTile, gi.it.ntok - gi.j * kUmmaTile);
+      t.nv = min(TT, gi.it.ntok - gi.j * TT);
       t.u = 0;
       t.ug = ug++;
       t.qi = gi.items;
