@@ -270,6 +270,17 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype,
  * clears it.  Like pa_decode_no_alloc, it allocates nothing. */
 pa_status pa_decode_no_alloc_error(void* stream, int32_t* device_status);
 
+/* Work-item shape of the tensor-core decode (bf16, head_dim 128), a
+ * process-wide planning setting: 0 = automatic (the default), 1 = one kv head
+ * per work item, 2 = two kv heads per item where the shape allows it (GQA
+ * group <= 4, an even kv-head count, blocks of 8..64 tokens; otherwise one).
+ * Two heads per item read each block of both heads with one tensor copy and
+ * halve the item count; the automatic choice takes them with about five
+ * two-head items per SM or more.  The result is the same either way up to
+ * fp32 rounding order.  The workspace size depends on the setting: size and
+ * decode under the same setting.  PA_ERR_INVALID_ARG for other values. */
+pa_status pa_set_decode_kv_per_item(int32_t kv_per_item);
+
 /* Partition size and CTA count pa_decode would use (host only; either out
  * pointer may be NULL). */
 pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

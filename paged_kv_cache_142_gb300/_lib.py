@@ -51,6 +51,7 @@ SIGNATURES = {
     "pa_decode_no_alloc": (i32, [vp, i32, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp, i32,
                                  vp, i32, C.c_float, i32, vp]),
     "pa_decode_no_alloc_error": (i32, [vp, P_i32]),
+    "pa_set_decode_kv_per_item": (i32, [i32]),
     "pa_decode_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, P_i32, P_i32]),
     "pa_workspace_init": (i32, [vp, C.c_size_t, vp]),
     "pa_test_stall_decode": (None, [C.c_uint64]),

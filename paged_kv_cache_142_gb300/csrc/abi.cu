@@ -51,6 +51,8 @@ using pa::DecodeParams;
 
 // Timeout-path test hook (pa_test_stall_decode): 0 = off.
 std::atomic<uint64_t> g_test_stall_ns{0};
+// kv heads per decode work item (pa_set_decode_kv_per_item): 0 = automatic.
+std::atomic<int> g_kv_per_item{0};
 
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kDefaultPartTokens = 256;
@@ -114,11 +116,15 @@ pa_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   pl->umma = dtype == PA_DTYPE_BF16 && head_dim == 128 && block_size >= 8 &&
              pa::decode_umma_fn(G, 1) != nullptr;
   // two kv heads per item: one TMA box per block covers both heads (twice the
-  // bytes per copy) and half as many items, with the same MMA shapes
-  pl->kh = pl->umma && G <= 4 && num_kv_heads % 2 == 0 && block_size <= 64 &&
-                   pa::decode_umma_fn(G, 2) != nullptr
-               ? 2
-               : 1;
+  // bytes per copy) and half as many items, with the same MMA shapes.  Taken
+  // only with about five such items per SM or more: with fewer, the longer
+  // items leave SMs idle at the end of the launch (GQA G = 4 sweep: one head
+  // per item wins up to 1024 sequence x kv-head pairs, two heads from 1536).
+  const int64_t pair_items = static_cast<int64_t>(num_seqs) * (num_kv_heads / 2);
+  const bool pairs_ok = pl->umma && G <= 4 && num_kv_heads % 2 == 0 && block_size <= 64 &&
+                        pa::decode_umma_fn(G, 2) != nullptr;
+  const int want_kh = g_kv_per_item.load(std::memory_order_relaxed);
+  pl->kh = pairs_ok && (want_kh == 2 || (want_kh == 0 && pair_items >= 5 * pa::device_sm_count())) ? 2 : 1;
   if (!pl->umma && !pa::decode_kernel_info(dtype == PA_DTYPE_BF16, head_dim, G, &pl->info))
     return PA_ERR_UNSUPPORTED;
   // partition size: a multiple of the block size and of the stage (tensor
@@ -780,6 +786,12 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, int32_t num_se
                          args, static_cast<size_t>(pl.smem), static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_set_decode_kv_per_item(int32_t kv_per_item) {
+  if (kv_per_item < 0 || kv_per_item > 2) return PA_ERR_INVALID_ARG;
+  g_kv_per_item.store(kv_per_item, std::memory_order_relaxed);
+  return PA_OK;
 }
 
 void pa_test_stall_decode(uint64_t ns) {

@@ -216,6 +216,12 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, bloc
     return int(n)
 
 
+def pa_set_decode_kv_per_item(kv_per_item: int) -> None:
+    """Work-item shape of the tensor-core decode: 0 automatic, 1 or 2 kv heads
+    per item (process-wide; size the workspace under the same setting)."""
+    L.check(_LIB.pa_set_decode_kv_per_item(int(kv_per_item)), "pa_set_decode_kv_per_item")
+
+
 def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                    max_context_len, partition_tokens=0):
     """(partition tokens, CTAs) pa_decode would use on the current device."""

@@ -116,3 +116,25 @@ def test_checked_calls_need_a_status_word(lib):
     assert lib.pa_copy_blocks_checked(None, None, 8, 16, 2, 128, 1, None, 2, None, None) == L.PA_ERR_INVALID_ARG
     # the no-alloc status read needs somewhere to put it
     assert lib.pa_decode_no_alloc_error(None, None) == L.PA_ERR_INVALID_ARG
+
+
+def test_kv_per_item_setting_shapes_the_plan(lib):
+    """The work-item setting is validated, and it changes the workspace the
+    plan needs (one merge counter per item row) where two kv heads can pair."""
+    from paged_kv_cache_142_gb300 import _lib as L
+    assert lib.pa_set_decode_kv_per_item(3) == L.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_kv_per_item(-1) == L.PA_ERR_INVALID_ARG
+    try:
+        sizes = {}
+        for kh in (1, 2):
+            assert lib.pa_set_decode_kv_per_item(kh) == L.PA_OK
+            sizes[kh] = lib.pa_decode_workspace_size(256, 32, 8, 128, 16, 1, 4096, 0)
+        assert sizes[1] > sizes[2] > 0  # 2048 rows of counters against 1024
+        # a shape that cannot pair (odd kv heads) plans the same either way
+        odd = []
+        for kh in (1, 2):
+            lib.pa_set_decode_kv_per_item(kh)
+            odd.append(lib.pa_decode_workspace_size(256, 24, 3, 128, 16, 1, 4096, 0))
+        assert odd[0] == odd[1]
+    finally:
+        lib.pa_set_decode_kv_per_item(0)

@@ -70,6 +70,14 @@ def test_long_context_split_k_all_sequences(ops, bs):
         assert max_err(out, ref) <= TOL["bf16"]
 
 
+@pytest.fixture
+def kv_per_item(ops, request):
+    """Plans under the given work-item shape, automatic again afterwards."""
+    ops.pa_set_decode_kv_per_item(request.param)
+    yield request.param
+    ops.pa_set_decode_kv_per_item(0)
+
+
 EDGE_LENS = [0, 1, 7, 8, 15, 16, 17, 31, 32, 33, 63, 64, 65, 255, 256, 257, 511, 600, 1000]
 
 
@@ -78,9 +86,16 @@ EDGE_LENS = [0, 1, 7, 8, 15, 16, 17, 31, 32, 33, 63, 64, 65, 255, 256, 257, 511,
     ("bf16", 64, 8, 16), ("bf16", 64, 1, 1), ("bf16", 128, 1, 16), ("bf16", 128, 2, 8),
     ("bf16", 128, 4, 16), ("bf16", 128, 8, 32), ("bf16", 256, 4, 16), ("bf16", 256, 8, 64),
     ("bf16", 128, 16, 16), ("bf16", 128, 4, 256),
+    # two kv heads per item with blocks of 32 and 64 tokens (a warp's rows all
+    # belong to one kv head there)
+    ("bf16", 128, 4, 32), ("bf16", 128, 2, 64), ("bf16", 128, 1, 64),
 ])
 @pytest.mark.parametrize("partition_tokens", [0, 64])
-def test_shape_sweep_edge_lengths(ops, dtype, D, G, bs, partition_tokens):
+@pytest.mark.parametrize("kv_per_item", [0, 1, 2], indirect=True)
+def test_shape_sweep_edge_lengths(ops, dtype, D, G, bs, partition_tokens, kv_per_item):
+    """Edge lengths over dtype x head_dim x G x block size; each case with the
+    automatic work-item shape and with one and two kv heads per item forced
+    (two only where the shape allows it)."""
     Hkv = 2
     wl = W.custom(f"sweep_{dtype}_{D}_{G}_{bs}", dtype, EDGE_LENS, G * Hkv, Hkv, D, bs,
                   pool_factor=1.3, seed=D * 10 + G + bs)
@@ -91,7 +106,8 @@ def test_shape_sweep_edge_lengths(ops, dtype, D, G, bs, partition_tokens):
     assert not to_f64(out)[0].any()  # the empty sequence gives zeros
 
 
-def test_block_permutation_invariance_bit_identical(ops):
+@pytest.mark.parametrize("kv_per_item", [1, 2], indirect=True)
+def test_block_permutation_invariance_bit_identical(ops, kv_per_item):
     """Other physical placement, same logical content: identical bits."""
     base = W.gqa_bf16(num_seqs=32)
     outs = []
@@ -162,3 +178,13 @@ def test_batch256_repeated_calls_bit_identical(ops, gqa_full, partition_tokens):
     for _ in range(12):
         assert torch.equal(g.decode(partition_tokens=partition_tokens, workspace=ws), first)
     assert max_err(first, ref) <= TOL["bf16"]
+
+
+def test_odd_kv_head_count_keeps_one_head_per_item(ops):
+    """Three kv heads cannot pair up: the tensor-core kernel runs one kv head
+    per item, and the result still matches the oracle."""
+    wl = W.custom("odd_kv", "bf16", [0, 1, 17, 200, 777, 1500], 6, 3, 128, 16, seed=31)
+    g = GpuState(wl, ops)
+    ref = OracleState(wl).decode()
+    for pt in (0, 64):
+        assert max_err(g.decode(partition_tokens=pt), ref) <= TOL["bf16"]
