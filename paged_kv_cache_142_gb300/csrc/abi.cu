@@ -82,7 +82,7 @@ constexpr int kUmmaTileBytesHost = 32768;
 // per compute group scratch of the tensor-core decode (with an item's totals for G >= 8)
 // (must match umma_small_bytes in decode_umma.cuh)
 constexpr int umma_small_bytes_host(int HG, int kh) { return (HG >= 8 || kh == 2) ? 1280 : 1024; }
-constexpr int kPrefillThreads = 288;  // must match the prefill kernel
+constexpr int kPrefillThreads = 256;  // must match the prefill kernel
 
 struct Plan {
   DecodeKernelInfo info;

@@ -15,14 +15,15 @@
 //   S[128 rows x 128 keys]   = Q[128 x 128 dims] . K_tile^T
 //   O[128 rows x 128 dims]  += P[128 x 128 keys] . V_tile
 // each eight tcgen05.mma (M = N = 128, K = 16) with fp32 accumulators in
-// tensor memory (S double-buffered, then O).  P enters the second product as
-// bf16 hi = bf16(p) and lo = bf16(p - hi), two passes of eight MMAs, so each
-// probability keeps about 16 bits.  P is written back into tensor memory
-// over the S tile it came from and read from there as the A operand of P.V,
-// so the two S buffers double-buffer P as well: the softmax of tile t + 1
-// runs while P.V of tile t is in flight.
+// tensor memory (three S buffers, then O).  P enters the second product as
+// bf16 hi = bf16(p) and lo = bf16(p - hi), sixteen MMAs into the one O, so
+// each probability keeps about 16 bits.  P is written back into tensor
+// memory over the S tile it came from and read from there as the A operand
+// of P.V, so the S buffers hold P as well.  With three of them, Q.K^T of
+// tile t + 1 waits only for P.V of tile t - 2: the next S is usually ready
+// when the softmax of tile t ends, while P.V of t and t - 1 are in flight.
 //
-// One CTA per SM, 288 threads, persistent over (tile of TQ tokens, sequence,
+// One CTA per SM, 256 threads, persistent over (tile of TQ tokens, sequence,
 // kv head) items, in blocks of a few (sequence, kv head) pairs so that the
 // CTAs at work share those pairs' keys and values in L2, later (longer) tiles
 // first within a block:
@@ -32,10 +33,9 @@
 //    into a ring of kRingStages; warp 2 loads the V tiles likewise;
 //  * warp 1 issues Q.K^T of every tile as soon as its K tile has landed and
 //    an S buffer is free (so the softmax of tile t overlaps Q.K^T of t + 1);
-//  * warps 3 and 8 issue P.V of the hi and the lo halves of P into two O
-//    accumulators in parallel (one thread issues an MMA about every hundred
-//    cycles), warp 3 zeroing first the V rows past the end inside the last
-//    16-key step of the item's last tile;
+//  * warp 3 issues P.V, per 16-key step the hi then the lo half of P, in a
+//    fixed order so the fp32 sums are reproducible, zeroing first the V rows
+//    past the end inside the last 16-key step of the item's last tile;
 //  * warps 4-7 own tensor-memory lanes 0-127, one query row per thread: per
 //    tile they read the row of S from tensor memory (max, then the
 //    exponentials), mask keys past the row's position, run the online
@@ -59,7 +59,7 @@ namespace pa {
 
 namespace prefill_detail {
 
-constexpr int kThreads = 288;  // 9 warps
+constexpr int kThreads = 256;  // 8 warps
 constexpr int kTileBytes = 32768;
 constexpr int kRingStages = 2;               // K ring and V ring depth
 constexpr int kOffQ = 0;                     // 2 query buffers (consecutive items)
@@ -69,16 +69,19 @@ constexpr int kOffBar = kOffV + kRingStages * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align the base
 constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only past 2^8
 
+constexpr int kNumS = 3;                     // S buffers in tensor memory
+
 // barriers
-// [S buffer]: kSFull (Q.K^T done), kPFull (P stored over S), kSFree (both
-// P.V passes of the tile done: S, P and every earlier O update are free)
+// [S buffer]: kSFull (Q.K^T done), kPFull (P stored over S), kSFree (P.V of
+// the tile done: S, P and every earlier O update are free)
 constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = kKFull + kRingStages,
               kVFull = kKEmpty + kRingStages, kVEmpty = kVFull + kRingStages, kSFull = kVEmpty + kRingStages,
-              kSFree = kSFull + 2, kPFull = kSFree + 2, kOEmpty = kPFull + 2, kDrain = kOEmpty + 1,
-              kVZero = kDrain + 3, kNumBars = kVZero + 1;  // drains: Q.K^T, P.V hi, P.V lo; then V-tail zeroed
+              kSFree = kSFull + kNumS, kPFull = kSFree + kNumS, kOEmpty = kPFull + kNumS, kDrain = kOEmpty + 1,
+              kNumBars = kDrain + 2;  // drains: Q.K^T, P.V
 static_assert(kNumBars * 8 + 8 + 4 <= 256, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-constexpr uint32_t kColO = 256;  // O from the hi halves of P; the lo halves' O at kColO + 128
+constexpr uint32_t kColO = kNumS * 128;  // O after the S buffers
+static_assert(kColO + 128 <= 512, "tensor memory columns");
 
 struct Item {
   int seq, kvh, qb, tok0, ntq, pos0, k_start, kend, ntiles, trow_seq, causal, part;
@@ -266,21 +269,20 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       ptx::mbar_init(&bars[kKFull + s], 1);
       ptx::mbar_init(&bars[kKEmpty + s], 1);
       ptx::mbar_init(&bars[kVFull + s], 1);
-      ptx::mbar_init(&bars[kVEmpty + s], 2);  // both P.V warps
+      ptx::mbar_init(&bars[kVEmpty + s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kNumS; ++s) {
       ptx::mbar_init(&bars[kSFull + s], 1);
-      ptx::mbar_init(&bars[kSFree + s], 2);  // both P.V warps
+      ptx::mbar_init(&bars[kSFree + s], 1);
       ptx::mbar_init(&bars[kPFull + s], 4);
     }
     ptx::mbar_init(&bars[kOEmpty], 4);
-    for (int d = 0; d < 3; ++d) ptx::mbar_init(&bars[kDrain + d], 1);
-    ptx::mbar_init(&bars[kVZero], 1);
+    for (int d = 0; d < 2; ++d) ptx::mbar_init(&bars[kDrain + d], 1);
     flags[0] = 0;
     ptx::mbar_init_fence();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, 512);  // S[2] x 128 columns, then O (hi, lo) x 128
+    ptx::tmem_alloc(tmem_slot, 512);  // S[3] x 128 columns, then O x 128
     ptx::tc_fence_before();
   }
   __syncthreads();
@@ -356,10 +358,10 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         const unsigned char* qt = qbuf + qs * 32768;
         wait(&bars[kQFull + qs], (ic >> 1) & 1u, aborted);
         for (int t = 0; t < it.ntiles && !aborted; ++t, ++kc, ++sc) {
-          const int b = static_cast<int>(sc & 1u);
+          const int b = static_cast<int>(sc % kNumS);
           const int kslot = static_cast<int>(kc % kRingStages);
           wait(&bars[kKFull + kslot], (kc / kRingStages) & 1u, aborted);
-          wait(&bars[kSFree + b], ((sc >> 1) & 1u) ^ 1u, aborted);
+          wait(&bars[kSFree + b], ((sc / kNumS) & 1u) ^ 1u, aborted);
           if (aborted) break;
           ptx::tc_fence_after();
           const unsigned char* kt = kring + kslot * kTileBytes;
@@ -386,56 +388,48 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       if (aborted || drain_aborted) flags[0] = 1;
     }
     __syncwarp();
-  } else if (warp == 3 || warp == 8) {
-    // ============ P.V issue: warp 3 the hi halves of P, warp 8 the lo ============
-    // Each accumulates into its own O (columns kColO / kColO + 128), so the
-    // two chains issue in parallel; the epilogue adds them.  P is the A
-    // operand, read from the tile's S buffer in tensor memory.
+  } else if (warp == 3) {
+    // ============================ P.V issue ============================
+    // Per 16-key step, the hi half of P then the lo half into the one O
+    // accumulator, in a fixed order, so the sums are reproducible.  P is
+    // the A operand, read from the tile's S buffer in tensor memory.
     constexpr uint32_t kIdPV = ptx::idesc_bf16_f32(128, 128, 0, 1);
-    const bool lo = warp == 8;
-    const uint32_t od = tmem + kColO + (lo ? 128u : 0u);
-    uint32_t ic = 0, vc = 0, tc = 0, zc = 0;
+    const uint32_t od = tmem + kColO;
+    uint32_t ic = 0, vc = 0, tc = 0;
     for (int w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
       Item it;
       if (!item_at(p, w, G, it)) continue;
       for (int t = 0; t < it.ntiles; ++t, ++vc, ++tc) {
         const int vslot = static_cast<int>(vc % kRingStages);
-        const int b = static_cast<int>(tc & 1u);
+        const int b = static_cast<int>(tc % kNumS);
         unsigned char* vt = vring + vslot * kTileBytes;
         if (lane == 0) {
           wait(&bars[kVFull + vslot], (vc / kRingStages) & 1u, aborted);
-          wait(&bars[kPFull + b], (tc >> 1) & 1u, aborted);
+          wait(&bars[kPFull + b], (tc / kNumS) & 1u, aborted);
           if (t == 0) wait(&bars[kOEmpty], (ic & 1u) ^ 1u, aborted);
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);
         if (aborted) break;
         const int nv = min(128, it.kend - it.k_start - t * 128);
         const int nks = (nv + 15) / 16;
-        if (nv & 15) {  // V rows past the end inside the last 16-key step: zeroed by warp 3
-          if (!lo) {
-            const int nrows = nks * 16 - nv;
-            for (int c = lane; c < nrows * 16; c += 32) {
-              const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
-              *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars[kVZero]);
-          } else {
-            if (lane == 0) wait(&bars[kVZero], zc & 1u, aborted);  // warp 3 has zeroed the rows
-            aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        if (nv & 15) {  // V rows past the end inside the last 16-key step: zeroed
+          const int nrows = nks * 16 - nv;
+          for (int c = lane; c < nrows * 16; c += 32) {
+            const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+            *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
           }
-          ++zc;
-          if (aborted) break;
+          ptx::fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) {
           ptx::tc_fence_after();
-          const uint32_t pa = tmem + static_cast<uint32_t>(b * 128) + (lo ? 8u : 0u);
-          for (int ks = 0; ks < nks; ++ks)
-            umma_ts_bf16(od, pa + ks * 16, ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128),
-                         kIdPV, t > 0 || ks > 0);
+          const uint32_t pa = tmem + static_cast<uint32_t>(b * 128);
+          for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t vd = ptx::smem_desc(vt + ks * 4096, 1024, 2048, ptx::kLayoutSw128);
+            umma_ts_bf16(od, pa + ks * 16, vd, kIdPV, t > 0 || ks > 0);
+            umma_ts_bf16(od, pa + ks * 16 + 8, vd, kIdPV, 1u);
+          }
           ptx::umma_commit(&bars[kSFree + b]);
           ptx::umma_commit(&bars[kVEmpty + vslot]);
         }
@@ -444,9 +438,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       ++ic;
     }
     if (lane == 0) {
-      ptx::umma_commit(&bars[kDrain + (lo ? 2 : 1)]);
+      ptx::umma_commit(&bars[kDrain + 1]);
       bool drain_aborted = false;
-      wait(&bars[kDrain + (lo ? 2 : 1)], 0, drain_aborted);
+      wait(&bars[kDrain + 1], 0, drain_aborted);
       if (aborted || drain_aborted) flags[0] = 1;
     }
     __syncwarp();
@@ -517,7 +511,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
     // item.  It runs after the next item's first softmax tile, so that P.V
     // is usually done by then and the wait costs nothing.
     auto epilogue = [&](const Item& eit, bool evalid, float em, float el, uint32_t last_sc) -> bool {
-      wait(&bars[kSFree + (last_sc & 1u)], (last_sc >> 1) & 1u, aborted);
+      wait(&bars[kSFree + last_sc % kNumS], (last_sc / kNumS) & 1u, aborted);
       aborted = __any_sync(0xffffffffu, aborted);
       if (aborted) return false;
       ptx::tc_fence_after();
@@ -532,12 +526,9 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32], vl[32];
+        uint32_t v[32];
         ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
-        ptx::TmemLd<32>::run(tmem + lane_base + kColO + 128 + c * 32, vl);
         ptx::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
         if (evalid && partial) {
           float4* dst = reinterpret_cast<float4*>(p.part_o + (slot_rows + prow) * 128 + c * 32);
 #pragma unroll
@@ -582,8 +573,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       const int limit = !valid ? 0 : (it.causal ? it.pos0 + trow + 1 : it.kend);
       float m_ref = -CUDART_INF_F, l = 0.f;
       for (int t = 0; t < it.ntiles; ++t) {
-        const int b = static_cast<int>(sc & 1u);
-        wait(&bars[kSFull + b], (sc >> 1) & 1u, aborted);
+        const int b = static_cast<int>(sc % kNumS);
+        wait(&bars[kSFull + b], (sc / kNumS) & 1u, aborted);
         aborted = __any_sync(0xffffffffu, aborted);
         if (aborted) break;
         ptx::tc_fence_after();
@@ -617,11 +608,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         if (__any_sync(0xffffffffu, rescale)) {
           // warp-collective rescale of both O in tensor memory, once P.V of
           // the previous tile (and so every earlier one) has landed in O
-          const uint32_t pb = (sc - 1u) & 1u;
-          wait(&bars[kSFree + pb], ((sc - 1u) >> 1) & 1u, aborted);
+          const uint32_t pb = (sc - 1u) % kNumS;
+          wait(&bars[kSFree + pb], ((sc - 1u) / kNumS) & 1u, aborted);
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
             ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
             ptx::tmem_wait_ld();
