@@ -509,8 +509,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       ptx::tmem_st32(dst, w);
     };
     // An item's epilogue: its O row divided by the row sum and stored, once
-    // its last P.V (tile last_sc) has landed; then O is handed to the next
-    // item.  It runs after the next item's first softmax tile, so that P.V
+    // its last P.V (tile last_sc) has landed.  O is handed to the next item
+    // as soon as its last chunk is read, before that chunk's stores.  It runs after the next item's first softmax tile, so that P.V
     // is usually done by then and the wait costs nothing.
     auto epilogue = [&](const Item& eit, bool evalid, float em, float el, uint32_t last_sc) -> bool {
       wait(&bars[kSFree + last_sc % kNumS], (last_sc / kNumS) & 1u, aborted);
@@ -531,6 +531,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         uint32_t v[32];
         ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
         ptx::tmem_wait_ld();
+        if (c == 3) {  // O is read: the next item's P.V may start
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
+        }
         if (evalid && partial) {
           float4* dst = reinterpret_cast<float4*>(p.part_o + (slot_rows + prow) * 128 + c * 32);
 #pragma unroll
@@ -557,9 +562,6 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
       return true;
     };
     bool pending = false;  // an item whose epilogue is still to run
