@@ -471,6 +471,22 @@ bool encode_q_tokens(CUtensorMap* m, const void* base, uint64_t tokens, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the bf16 output [num_tokens][num_heads][128]: boxes of 64
+// elements (one 128-byte swizzle span) x hb heads x tb tokens, the rows of
+// one softmax warp of the prefill kernel (hb * tb = 32).
+bool encode_out_tokens(CUtensorMap* m, void* base, uint64_t tokens, uint64_t heads, uint32_t hb,
+                       uint32_t tb) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, heads, tokens};
+  cuuint64_t strides[2] = {256, heads * 256};
+  cuuint32_t box[3] = {64, hb, tb};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The tensor-core prefill kernel over `items` work items (any mode).
 pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void* q,
                          const void* k_cache, const void* v_cache, int64_t cache_rows,
@@ -503,7 +519,16 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
       !encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
       !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows))
     return PA_ERR_CUDA;
-  void* args[] = {&p, &tmq, &tmk, &tmv};
+  // causal prefill into bf16: full tiles' rows leave through shared memory
+  // and TMA stores (a 16-byte aligned output; else plain stores)
+  CUtensorMap tmo = tmq;
+  const uint32_t tq = static_cast<uint32_t>(128 / G);
+  p.o_tma = p.mode == 0 && p.out_bf16 && (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0 &&
+            encode_out_tokens(&tmo, p.out, static_cast<uint64_t>(p.num_tokens),
+                              static_cast<uint64_t>(p.num_q_heads), tq >= 32 ? 1u : 32u / tq,
+                              tq >= 32 ? 32u : tq);
+  if (!p.o_tma) tmo = tmq;
+  void* args[] = {&p, &tmq, &tmk, &tmv, &tmo};
   cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(kPrefillThreads), args,
                                    static_cast<size_t>(smem), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -44,7 +44,9 @@
 //    running max is the reference of P and O and is raised only when a row's
 //    max grows by more than 2^8 (then the warp rescales its O rows in tensor
 //    memory), so most tiles leave O alone.  At the item's end each thread
-//    divides its O row by the row sum and stores it.
+//    divides its O row by the row sum; into bf16, a warp whose 32 rows are
+//    all valid writes them to its 8 KB of shared memory and stores them with
+//    two TMA stores, other rows are stored one by one.
 // Every mbarrier wait is bounded; on expiry the roles stop, the issuer
 // drains, tensor memory is freed and PA_ERR_DEVICE_TIMEOUT is written to the
 // caller's status word.
@@ -66,7 +68,8 @@ constexpr int kOffQ = 0;                     // 2 query buffers (consecutive ite
 constexpr int kOffK = 65536;
 constexpr int kOffV = kOffK + kRingStages * kTileBytes;
 constexpr int kOffBar = kOffV + kRingStages * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align the base
+constexpr int kOffStage = kOffBar + 1024;        // 4 x 8 KB: a softmax warp's output rows
+constexpr int kSmemBytes = kOffStage + 4 * 8192 + 1024;  // then slack to align the base
 constexpr float kRescaleLog2 = 8.0f;          // raise the reference max only past 2^8
 
 constexpr int kNumS = 3;                     // S buffers in tensor memory
@@ -238,7 +241,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
     paged_prefill_umma_kernel(const __grid_constant__ PrefillParams p,
                               const __grid_constant__ CUtensorMap tm_q,
                               const __grid_constant__ CUtensorMap tm_k,
-                              const __grid_constant__ CUtensorMap tm_v) {
+                              const __grid_constant__ CUtensorMap tm_v,
+                              const __grid_constant__ CUtensorMap tm_o) {
   using namespace prefill_detail;
   static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
   constexpr int TQ = 128 / G;
@@ -526,6 +530,47 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         p.part_ml[(slot_rows + prow) * 2] = em;
         p.part_ml[(slot_rows + prow) * 2 + 1] = el;
       }
+      if (p.o_tma && __all_sync(0xffffffffu, evalid)) {
+        // The warp's 32 rows, scaled and rounded to bf16, into its 8 KB of
+        // shared memory in the output map's box order (token-major, then
+        // head; two 64-dim halves, 128-byte swizzled), then two TMA stores.
+        constexpr int HB = TQ >= 32 ? 1 : 32 / TQ;  // heads in the warp's box
+        const int brow = TQ >= 32 ? lane : (lane % TQ) * HB + lane / TQ;
+        unsigned char* stg = smem + kOffStage + quarter * 8192;
+        if (lane == 0) ptx::bulk_wait_read();  // the previous item's stores have read it
+        __syncwarp();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
+          ptx::tmem_wait_ld();
+          if (c == 3) {  // O is read: the next item's P.V may start
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
+          }
+          unsigned char* line = stg + (c >> 1) * 4096 + brow * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+            const int chunk = ((c & 1) * 4 + q) ^ (brow & 7);
+            *reinterpret_cast<uint4*>(line + chunk * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int r0 = 32 * quarter;
+          const int y = eit.kvh * G + r0 / TQ, z = eit.qb + eit.tok0 + r0 % TQ;
+          ptx::tma_store_3d(&tm_o, stg, 0, y, z);
+          ptx::tma_store_3d(&tm_o, stg + 4096, 64, y, z);
+          ptx::bulk_commit();
+        }
+        return true;
+      }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -659,6 +704,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       psc = sc - 1u;
     }
     if (pending && !aborted) epilogue(pit, pvalid, pm, pl, psc);
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's output stores are complete
   }
 
   // ============================ teardown ============================

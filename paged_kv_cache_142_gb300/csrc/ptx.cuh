@@ -146,6 +146,24 @@ __device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tensor_m
       : "memory");
 }
 
+// 3-D tiled TMA store of one box from shared memory at coordinates (x =
+// inner element, y, z), in this thread's bulk group.  The shared memory may
+// be rewritten once bulk_wait_read() has returned.
+__device__ __forceinline__ void tma_store_3d(const void* tensor_map, const void* src_smem, int x, int y,
+                                             int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   tensor_map),
+               "r"(smem_addr(src_smem)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk groups have finished reading their shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk groups are complete (their global writes done)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const void* tensor_map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tensor_map) : "memory");
 }

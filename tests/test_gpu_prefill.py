@@ -83,6 +83,21 @@ def test_prefill_bf16_output_and_long_prompt(ops):
     assert (np.abs(got - ref) <= np.maximum(TOL["bf16"], TOL["bf16"] + bf16_half_ulp(ref))).all()
 
 
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_prefill_bf16_output_every_group(ops, G):
+    """bf16 output for every GQA group size: a tile's rows leave in boxes of
+    one warp's 32 rows (32 tokens of one head for 128 / G >= 32, else 128 / G
+    tokens of 32 G / 128 heads) when all of them are valid, row by row
+    otherwise; the chunks mix whole tiles and ragged ends."""
+    c = _case(G, 16, [(0, 300), (40, 256), (0, 129), (5, 3)], seed=31 + G)
+    out, ref, st = _run(ops, c, out_dtype=torch.bfloat16)
+    assert st == 0
+    got = to_f64(out)
+    from paged_case import bf16_half_ulp
+    assert np.isfinite(got).all()
+    assert (np.abs(got - ref) <= np.maximum(TOL["bf16"], TOL["bf16"] + bf16_half_ulp(ref))).all()
+
+
 def test_chunked_prefill_equals_whole(ops):
     """The same prompt in one call and in three pieces (later starts)."""
     whole = _case(4, 16, [(0, 257)], seed=9)
