@@ -540,23 +540,24 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         if (lane == 0) ptx::bulk_wait_read();  // the previous item's stores have read it
         __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          ptx::TmemLd<32>::run(tmem + lane_base + kColO + c * 32, v);
+        for (int hh = 0; hh < 2; ++hh) {  // one 64-dim half per tensor-memory wait
+          uint32_t v[64];
+          ptx::TmemLd<32>::run(tmem + lane_base + kColO + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+          ptx::TmemLd<32>::run(tmem + lane_base + kColO + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
           ptx::tmem_wait_ld();
-          if (c == 3) {  // O is read: the next item's P.V may start
+          if (hh == 1) {  // O is read: the next item's P.V may start
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
           }
-          unsigned char* line = stg + (c >> 1) * 4096 + brow * 128;
+          unsigned char* line = stg + hh * 4096 + brow * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 8; ++q) {
             uint32_t w4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
-            const int chunk = ((c & 1) * 4 + q) ^ (brow & 7);
+            const int chunk = q ^ (brow & 7);
             *reinterpret_cast<uint4*>(line + chunk * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
