@@ -471,20 +471,21 @@ bool encode_q_tokens(CUtensorMap* m, const void* base, uint64_t tokens, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over the bf16 output [num_tokens][num_heads][128]: boxes of 64
-// elements (one 128-byte swizzle span) x hb heads x tb tokens, the rows of
-// one softmax warp of the prefill kernel (hb * tb = 32).
-bool encode_out_tokens(CUtensorMap* m, void* base, uint64_t tokens, uint64_t heads, uint32_t hb,
-                       uint32_t tb) {
+// 3-D map over output rows [tokens][num_heads][128] of bf16 or fp32: boxes
+// of one 128-byte swizzle span (64 bf16 or 32 fp32 elements) x hb heads x tb
+// tokens, the rows of one softmax warp of the prefill kernel (hb * tb = 32).
+bool encode_out_rows(CUtensorMap* m, void* base, bool fp32, uint64_t tokens, uint64_t heads, uint32_t hb,
+                     uint32_t tb) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
+  const uint64_t row = fp32 ? 512 : 256;
   cuuint64_t dims[3] = {128, heads, tokens};
-  cuuint64_t strides[2] = {256, heads * 256};
-  cuuint32_t box[3] = {64, hb, tb};
+  cuuint64_t strides[2] = {row, heads * row};
+  cuuint32_t box[3] = {fp32 ? 32u : 64u, hb, tb};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The tensor-core prefill kernel over `items` work items (any mode).
@@ -493,7 +494,9 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
                          void* stream) {
   if (items >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
   if (items == 0) return PA_OK;
-  const void* fn = pa::prefill_umma_fn(G);
+  // fp32 rows: the output of an fp32 prefill, or the shared-prefix partials
+  const bool fp32_rows = p.mode != 0 || !p.out_bf16;
+  const void* fn = pa::prefill_umma_fn(G, fp32_rows);
   const int smem = pa::prefill_umma_smem_bytes();
   int ctas = 0;
   pa_status st = prepare_kernel(fn, kPrefillThreads, smem, &ctas);
@@ -519,15 +522,21 @@ pa_status launch_prefill(pa::PrefillParams& p, int G, int64_t items, const void*
       !encode_kv_groups(&tmk, k_cache, static_cast<uint64_t>(cache_rows), box_rows) ||
       !encode_kv_groups(&tmv, v_cache, static_cast<uint64_t>(cache_rows), box_rows))
     return PA_ERR_CUDA;
-  // causal prefill into bf16: full tiles' rows leave through shared memory
-  // and TMA stores (a 16-byte aligned output; else plain stores)
+  // full tiles' rows leave through shared memory and TMA stores: the bf16 or
+  // fp32 output of a causal prefill, or the shared-prefix passes' fp32
+  // partial O [parts + 1][num_seqs][num_q_heads][128] (else plain stores)
   CUtensorMap tmo = tmq;
   const uint32_t tq = static_cast<uint32_t>(128 / G);
-  p.o_tma = p.mode == 0 && p.out_bf16 && (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0 &&
-            encode_out_tokens(&tmo, p.out, static_cast<uint64_t>(p.num_tokens),
-                              static_cast<uint64_t>(p.num_q_heads), tq >= 32 ? 1u : 32u / tq,
-                              tq >= 32 ? 32u : tq);
-  if (!p.o_tma) tmo = tmq;
+  void* obase = p.mode == 0 ? p.out : static_cast<void*>(p.part_o);
+  const uint64_t orows = p.mode == 0 ? static_cast<uint64_t>(p.num_tokens)
+                                     : static_cast<uint64_t>(p.num_parts + 1) * static_cast<uint64_t>(p.num_seqs);
+  p.o_tma = 0;
+  if ((reinterpret_cast<uintptr_t>(obase) & 15u) == 0 &&
+      encode_out_rows(&tmo, obase, fp32_rows, orows, static_cast<uint64_t>(p.num_q_heads),
+                      tq >= 32 ? 1u : 32u / tq, tq >= 32 ? 32u : tq))
+    p.o_tma = fp32_rows ? 2 : 1;
+  else
+    tmo = tmq;
   void* args[] = {&p, &tmq, &tmk, &tmv, &tmo};
   cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(kPrefillThreads), args,
                                    static_cast<size_t>(smem), static_cast<cudaStream_t>(stream));
@@ -592,6 +601,11 @@ int64_t cascade_part_tokens(int64_t max_prefix, int64_t items_per_part) {
 }
 }  // namespace
 
+// The partial-result scratch holds (max, sum) per (part, row), then the
+// unnormalised O rows; the O part starts 256 bytes in, so that its 512-byte
+// rows stay 16-byte aligned (vector and TMA stores) for any row count.
+static int64_t cascade_ml_floats(int64_t parts, int64_t rows) { return round_up((parts + 1) * rows * 2, 64); }
+
 size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                               int32_t num_kv_heads, int32_t num_groups,
                                               int32_t max_group_size, int32_t max_prefix_len) {
@@ -604,7 +618,7 @@ size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_he
   const int64_t pt = cascade_part_tokens(max_prefix_len, static_cast<int64_t>(num_groups) * num_kv_heads * tiles);
   const int64_t parts = (max_prefix_len + pt - 1) / pt;
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
-  return static_cast<size_t>((parts + 1) * rows * (2 + 128) * 4 + 256);
+  return static_cast<size_t>((cascade_ml_floats(parts, rows) + (parts + 1) * rows * 128) * 4 + 256);
 }
 
 pa_status pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, int32_t num_seqs,
@@ -666,7 +680,7 @@ pa_status pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, 
   p.part_tokens = static_cast<int32_t>(pt);
   p.num_parts = static_cast<int32_t>(parts);
   p.part_ml = static_cast<float*>(workspace);
-  p.part_o = p.part_ml + (parts + 1) * rows * 2;
+  p.part_o = p.part_ml + cascade_ml_floats(parts, rows);
   // one launch: the groups' prefixes (every member's queries against each
   // prefix block once), then every member's own tokens past its group's prefix
   p.mode = 3;

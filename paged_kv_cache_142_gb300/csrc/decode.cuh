@@ -93,7 +93,7 @@ struct PrefillParams {
   int32_t num_tokens;
   int32_t tiles_per_seq;   // ceil(max chunk length / tokens per tile)
   int32_t pair_block;      // mode 0: (sequence, kv head) pairs per block of the item order
-  int32_t o_tma;           // mode 0, bf16 out: a warp's rows of a full tile leave by TMA stores
+  int32_t o_tma;           // a warp's rows of a full tile leave by TMA stores: 1 bf16, 2 fp32 rows
   float scale_log2;
   int32_t* status;         // device error word (may be null)
   // shared-prefix decode (mode 1: the groups' prefixes, mode 2: the members'
@@ -109,7 +109,7 @@ struct PrefillParams {
   float* part_ml;               // [num_parts + 1][num_seqs * num_q_heads][2]: max (log2), sum
   float* part_o;                // [num_parts + 1][num_seqs * num_q_heads][128]: unnormalised O
 };
-const void* prefill_umma_fn(int group);
+const void* prefill_umma_fn(int group, bool fp32_rows = false);
 int prefill_umma_smem_bytes();
 cudaError_t launch_cascade_merge(const PrefillParams& p, cudaStream_t stream);
 

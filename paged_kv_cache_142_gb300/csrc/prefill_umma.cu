@@ -236,7 +236,10 @@ __device__ __forceinline__ void umma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, u
 
 }  // namespace prefill_detail
 
-template <int G>
+// F32: full tiles' rows leave as fp32 (the output, or the shared-prefix
+// partial O) by TMA stores; else as bf16 (the causal prefill's output).  Two
+// instantiations keep each epilogue's code out of the other's kernel.
+template <int G, bool F32>
 __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
     paged_prefill_umma_kernel(const __grid_constant__ PrefillParams p,
                               const __grid_constant__ CUtensorMap tm_q,
@@ -530,7 +533,50 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         p.part_ml[(slot_rows + prow) * 2] = em;
         p.part_ml[(slot_rows + prow) * 2 + 1] = el;
       }
-      if (p.o_tma && __all_sync(0xffffffffu, evalid)) {
+      if (F32 && p.o_tma == 2 && __all_sync(0xffffffffu, evalid)) {
+        // fp32 rows (the output, or the shared-prefix partial O): per 64-dim
+        // half, the warp's 32 rows into its 8 KB of shared memory as two
+        // boxes of 32 floats (128-byte swizzled), then two TMA stores
+        constexpr int HB = TQ >= 32 ? 1 : 32 / TQ;
+        const int brow = TQ >= 32 ? lane : (lane % TQ) * HB + lane / TQ;
+        unsigned char* stg = smem + kOffStage + quarter * 8192;
+        const int r0 = 32 * quarter;
+        const int y = eit.kvh * G + r0 / TQ;
+        const int z = (partial ? eit.part * p.num_seqs : 0) + eit.qb + eit.tok0 + r0 % TQ;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[64];
+          ptx::TmemLd<32>::run(tmem + lane_base + kColO + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+          ptx::TmemLd<32>::run(tmem + lane_base + kColO + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          ptx::tmem_wait_ld();
+          if (hh == 1) {  // O is read: the next item's P.V may start
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars[kOEmpty]);
+          }
+          if (lane == 0) ptx::bulk_wait_read();  // earlier stores have read the staging
+          __syncwarp();
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx) {
+            unsigned char* line = stg + bx * 4096 + brow * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float* f = reinterpret_cast<const float*>(v + 32 * bx + 4 * q);
+              *reinterpret_cast<float4*>(line + (q ^ (brow & 7)) * 16) =
+                  make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tm_o, stg, hh * 64, y, z);
+            ptx::tma_store_3d(&tm_o, stg + 4096, hh * 64 + 32, y, z);
+            ptx::bulk_commit();
+          }
+        }
+        return true;
+      }
+      if (!F32 && p.o_tma == 1 && __all_sync(0xffffffffu, evalid)) {
         // The warp's 32 rows, scaled and rounded to bf16, into its 8 KB of
         // shared memory in the output map's box order (token-major, then
         // head; two 64-dim halves, 128-byte swizzled), then two TMA stores.
@@ -774,13 +820,18 @@ cudaError_t launch_cascade_merge(const PrefillParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, cascade_merge_kernel, p);
 }
 
-const void* prefill_umma_fn(int group) {
+const void* prefill_umma_fn(int group, bool fp32_rows) {
   switch (group) {
-    case 1: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<1>);
-    case 2: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<2>);
-    case 4: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<4>);
-    case 8: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<8>);
-    case 16: return reinterpret_cast<const void*>(&paged_prefill_umma_kernel<16>);
+    case 1: return fp32_rows ? reinterpret_cast<const void*>(&paged_prefill_umma_kernel<1, true>)
+                             : reinterpret_cast<const void*>(&paged_prefill_umma_kernel<1, false>);
+    case 2: return fp32_rows ? reinterpret_cast<const void*>(&paged_prefill_umma_kernel<2, true>)
+                             : reinterpret_cast<const void*>(&paged_prefill_umma_kernel<2, false>);
+    case 4: return fp32_rows ? reinterpret_cast<const void*>(&paged_prefill_umma_kernel<4, true>)
+                             : reinterpret_cast<const void*>(&paged_prefill_umma_kernel<4, false>);
+    case 8: return fp32_rows ? reinterpret_cast<const void*>(&paged_prefill_umma_kernel<8, true>)
+                             : reinterpret_cast<const void*>(&paged_prefill_umma_kernel<8, false>);
+    case 16: return fp32_rows ? reinterpret_cast<const void*>(&paged_prefill_umma_kernel<16, true>)
+                              : reinterpret_cast<const void*>(&paged_prefill_umma_kernel<16, false>);
     default: return nullptr;
   }
 }

@@ -108,11 +108,13 @@ def test_beam_search_shared_prefix_decode(ops, bs):
             assert float(np.abs(to_f64(out) - to_f64(plain)).max()) <= 2 * TOL["bf16"]
 
 
-@pytest.mark.parametrize("G", [1, 4, 8])
-def test_random_groups(ops, G):
+@pytest.mark.parametrize("G,Hkv", [(1, 2), (4, 2), (8, 2), (1, 1)])
+def test_random_groups(ops, G, Hkv):
     """Groups of several sizes and prefix lengths, singletons without a
-    prefix, members whose length equals the prefix."""
-    bs, Hkv, D = 16, 2, 128
+    prefix, members whose length equals the prefix.  With one query head
+    and an odd number of sequences the partial-result rows are odd in
+    number, which the workspace layout must still keep 16-byte aligned."""
+    bs, D = 16, 128
     H = G * Hkv
     rng = np.random.default_rng(70 + G)
     NB = 900
