@@ -44,9 +44,11 @@
 //    running max is the reference of P and O and is raised only when a row's
 //    max grows by more than 2^8 (then the warp rescales its O rows in tensor
 //    memory), so most tiles leave O alone.  At the item's end each thread
-//    divides its O row by the row sum; into bf16, a warp whose 32 rows are
-//    all valid writes them to its 8 KB of shared memory and stores them with
-//    two TMA stores, other rows are stored one by one.
+//    divides its O row by the row sum (the shared-prefix passes keep it
+//    unnormalised, with the row's max and sum); a warp whose 32 rows are all
+//    valid writes them to its 8 KB of shared memory and stores them with TMA
+//    stores (bf16 or fp32 rows, one instantiation each), other rows are
+//    stored one by one.
 // Every mbarrier wait is bounded; on expiry the roles stop, the issuer
 // drains, tensor memory is freed and PA_ERR_DEVICE_TIMEOUT is written to the
 // caller's status word.
