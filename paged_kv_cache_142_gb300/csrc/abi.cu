@@ -684,8 +684,12 @@ pa_status pa_decode_shared_prefix(void* out, pa_dtype out_dtype, const void* q, 
   // one launch: the groups' prefixes (every member's queries against each
   // prefix block once), then every member's own tokens past its group's prefix
   p.mode = 3;
-  st = launch_prefill(p, G, parts * num_groups * num_kv_heads * tiles + static_cast<int64_t>(num_seqs) * num_kv_heads,
-                      q, k_cache, v_cache, cache_rows, stream);
+  // own-token items hold two members each (64-key halves of a tile) while a
+  // block's TMA box fits in a half
+  p.pack2 = block_size <= 64 ? 1 : 0;
+  const int64_t own_items = (p.pack2 ? (static_cast<int64_t>(num_seqs) + 1) / 2 : num_seqs) * num_kv_heads;
+  st = launch_prefill(p, G, parts * num_groups * num_kv_heads * tiles + own_items, q, k_cache, v_cache, cache_rows,
+                      stream);
   if (st != PA_OK) return st;
   // then the log-sum-exp merge into out
   cudaError_t e = pa::launch_cascade_merge(p, static_cast<cudaStream_t>(stream));

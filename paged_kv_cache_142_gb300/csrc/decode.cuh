@@ -94,6 +94,7 @@ struct PrefillParams {
   int32_t tiles_per_seq;   // ceil(max chunk length / tokens per tile)
   int32_t pair_block;      // mode 0: (sequence, kv head) pairs per block of the item order
   int32_t o_tma;           // a warp's rows of a full tile leave by TMA stores: 1 bf16, 2 fp32 rows
+  int32_t pack2;           // modes 2-3: two members per own-token item (block size <= 64)
   float scale_log2;
   int32_t* status;         // device error word (may be null)
   // shared-prefix decode (mode 1: the groups' prefixes, mode 2: the members'

@@ -90,6 +90,10 @@ static_assert(kColO + 128 <= 512, "tensor memory columns");
 
 struct Item {
   int seq, kvh, qb, tok0, ntq, pos0, k_start, kend, ntiles, trow_seq, causal, part;
+  // a packed own-token item: members qb and qb + 1, each in its own 64-key
+  // half of every tile, own tokens [k_start, k_start + own0) and
+  // [k_start1, k_start1 + own1) of their tables (rows trow_seq, trow_seq1)
+  int packed, own0, own1, k_start1, trow_seq1;
 };
 
 // The group of batch sequence i (group_start is non-decreasing).
@@ -116,7 +120,29 @@ __device__ __forceinline__ void bad_input(const PrefillParams& p) {
 __device__ __forceinline__ int prefix_items(const PrefillParams& p) {
   return p.num_parts * p.num_groups * p.num_kv_heads * p.tiles_per_seq;
 }
+__device__ __forceinline__ int own_items(const PrefillParams& p) {
+  return (p.pack2 ? (p.num_seqs + 1) / 2 : p.num_seqs) * p.num_kv_heads;
+}
+// Member m's own tokens [k_start, kend) past its group's prefix; false (and
+// the error reported) for inconsistent lengths or prefixes.
+__device__ __forceinline__ bool own_range(const PrefillParams& p, int m, int64_t table_tokens, int& k_start,
+                                          int& kend);
+__device__ __forceinline__ bool own_range(const PrefillParams& p, int m, int64_t table_tokens, int& k_start,
+                                          int& kend) {
+  const int grp = group_of(p, m);
+  const int P = p.prefix_len[grp];
+  const int len = p.context_lens[m];
+  if (len < 0 || len > p.max_context_len || static_cast<int64_t>(len) > table_tokens || P < 0 ||
+      P % p.block_size != 0 || P > len) {
+    bad_input(p);
+    return false;
+  }
+  k_start = P;
+  kend = len;
+  return true;
+}
 __device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, Item& it) {
+  it.packed = 0;
   const int hkv = p.num_kv_heads;
   const int TQ = 128 / G;
   const int64_t table_tokens = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
@@ -182,6 +208,32 @@ __device__ __forceinline__ bool item_at(const PrefillParams& p, int w, int G, It
     it.pos0 = 0;
     it.trow_seq = it.qb;  // the prefix blocks are the same in every member's table
     it.causal = 0;
+  } else if (p.pack2) {
+    // two members per item, each in a 64-key half of every tile
+    const int i = w / hkv;
+    it.kvh = w - i * hkv;
+    const int m0 = 2 * i, m1 = m0 + 1;
+    const bool has1 = m1 < p.num_seqs;
+    int e0 = 0, ks1 = 0, e1 = 0;
+    if (!own_range(p, m0, table_tokens, it.k_start, e0)) return false;
+    if (has1 && !own_range(p, m1, table_tokens, ks1, e1)) return false;
+    it.seq = m0;
+    it.qb = m0;
+    it.tok0 = 0;
+    it.ntq = has1 ? 2 : 1;
+    it.pos0 = 0;
+    it.kend = e0;
+    it.own0 = e0 - it.k_start;
+    it.own1 = has1 ? e1 - ks1 : 0;
+    it.k_start1 = ks1;
+    it.trow_seq = m0;
+    it.trow_seq1 = has1 ? m1 : m0;
+    it.causal = 0;
+    it.part = p.num_parts;
+    it.packed = 1;
+    if (it.own0 <= 0 && it.own1 <= 0) return false;  // no own tokens: the merge skips this part
+    it.ntiles = (max(it.own0, it.own1) + 63) / 64;
+    return true;
   } else {
     const int i = w / hkv;
     it.kvh = w - i * hkv;
@@ -266,8 +318,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
   const int bs_log = __ffs(bs) - 1;
   const int items = p.mode == 0   ? p.num_seqs * hkv * p.tiles_per_seq
                     : p.mode == 1 ? prefix_items(p)
-                    : p.mode == 2 ? p.num_seqs * hkv
-                                  : prefix_items(p) + p.num_seqs * hkv;
+                    : p.mode == 2 ? own_items(p)
+                                  : prefix_items(p) + own_items(p);
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -330,13 +382,31 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
       for (int t = 0; t < it.ntiles && !aborted; ++t, ++fc) {
         const int slot = static_cast<int>(fc % kRingStages);
         const uint32_t ph = (fc / kRingStages) & 1u;
-        const int nv = min(128, it.kend - it.k_start - t * 128);
-        const int nbox = (nv + box_rows - 1) / box_rows;
+        // this lane's box: of the tile (rows lane * box_rows ..), or in a
+        // packed item of member lane / 8's 64-key half (box lane % 8)
+        int nbox_total, tok = 0, dst_row = 0;
+        bool mine;
+        const int32_t* brow_tbl = trow;
+        if (F32 && it.packed) {
+          const int j = lane >> 3, bi = lane & 7;
+          const int n0 = min(64, max(0, it.own0 - t * 64)), n1 = min(64, max(0, it.own1 - t * 64));
+          const int nb0 = (n0 + box_rows - 1) / box_rows, nb1 = (n1 + box_rows - 1) / box_rows;
+          nbox_total = nb0 + nb1;
+          mine = lane < 16 && bi < (j ? nb1 : nb0);
+          tok = (j ? it.k_start1 : it.k_start) + t * 64 + bi * box_rows;
+          dst_row = j * 64 + bi * box_rows;
+          if (j) brow_tbl = p.block_tables + static_cast<int64_t>(it.trow_seq1) * p.max_blocks_per_seq;
+        } else {
+          const int nv = min(128, it.kend - it.k_start - t * 128);
+          nbox_total = (nv + box_rows - 1) / box_rows;
+          mine = lane < nbox_total;
+          tok = it.k_start + t * 128 + lane * box_rows;
+          dst_row = lane * box_rows;
+        }
         int row = 0;
-        if (lane < nbox) {
-          const int tok = it.k_start + t * 128 + lane * box_rows;
+        if (mine) {
           const int lb = tok >> bs_log;
-          int phys = trow[lb];
+          int phys = brow_tbl[lb];
           if (phys < 0 || phys >= p.num_blocks) {  // never read outside the pool
             if (p.status) atomicExch(p.status, kDevErrInvalidArg);
             phys = 0;
@@ -345,12 +415,11 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         }
         if (lane == 0) {
           wait(&empty[slot], ph ^ 1u, aborted);
-          ptx::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * box_rows * 256));
+          ptx::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox_total * box_rows * 256));
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);
-        if (!aborted && lane < nbox)
-          ptx::tma_load_4d(ring + slot * kTileBytes + lane * box_rows * 256, tm, 0, 0, 0, row >> 3,
-                           &full[slot], pol_kv);
+        if (!aborted && mine)
+          ptx::tma_load_4d(ring + slot * kTileBytes + dst_row * 256, tm, 0, 0, 0, row >> 3, &full[slot], pol_kv);
         __syncwarp();
       }
       ++ic;
@@ -421,16 +490,34 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);
         if (aborted) break;
-        const int nv = min(128, it.kend - it.k_start - t * 128);
-        const int nks = (nv + 15) / 16;
-        if (nv & 15) {  // V rows past the end inside the last 16-key step: zeroed
-          const int nrows = nks * 16 - nv;
-          for (int c = lane; c < nrows * 16; c += 32) {
-            const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
-            *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
-                make_uint4(0, 0, 0, 0);
+        int nks;
+        if (F32 && it.packed) {
+          // both 64-key halves take part: the rows past each member's own
+          // tokens in this tile are zeroed (P is 0 there; the rows may hold
+          // anything, even non-finite values)
+          nks = 8;
+#pragma unroll 1
+          for (int j = 0; j < 2; ++j) {
+            const int nvj = min(64, max(0, (j ? it.own1 : it.own0) - t * 64));
+            for (int c = lane; c < (64 - nvj) * 16; c += 32) {
+              const int rr = j * 64 + nvj + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+              *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
           }
           ptx::fence_proxy_async_smem();
+        } else {
+          const int nv = min(128, it.kend - it.k_start - t * 128);
+          nks = (nv + 15) / 16;
+          if (nv & 15) {  // V rows past the end inside the last 16-key step: zeroed
+            const int nrows = nks * 16 - nv;
+            for (int c = lane; c < nrows * 16; c += 32) {
+              const int rr = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+              *reinterpret_cast<uint4*>(vt + (rr >> 3) * 2048 + half * 1024 + (rr & 7) * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            ptx::fence_proxy_async_smem();
+          }
         }
         __syncwarp();
         if (lane == 0) {
@@ -678,8 +765,19 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * 128;
         const int key0 = it.k_start + t * 128;
-        // keys of this tile visible to the row: a prefix of nvis columns
-        const int nvis = min(128, max(0, limit - key0));
+        // keys of this tile visible to the row: a prefix of nvis columns; in a
+        // packed item, a prefix of the row's member's 64-key half
+        int nvis = min(128, max(0, limit - key0));
+        int half_own = -1;  // packed: the row's member's half (0, 1), else -1
+        if (F32 && it.packed) {
+          half_own = trow;
+          nvis = valid ? min(64, max(0, (trow ? it.own1 : it.own0) - t * 64)) : 0;
+        }
+        // visible columns of the 32-column chunk c, counted from its start
+        auto ncol = [&](int c) -> int {
+          if (F32 && half_own >= 0) return (c >> 1) == half_own ? nvis - (c & 1) * 32 : 0;
+          return nvis - c * 32;
+        };
         // pass 1: the row's max over its visible raw scores (scale > 0 keeps
         // the order), two 32-column chunks per tensor-memory wait
         float mraw = -CUDART_INF_F;
@@ -689,8 +787,8 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           ptx::TmemLd<32>::run(sbase + c * 32, va);
           ptx::TmemLd<32>::run(sbase + c * 32 + 32, vb);
           ptx::tmem_wait_ld();
-          mraw = fmaxf(mraw, chunk_max(va, nvis - c * 32));
-          mraw = fmaxf(mraw, chunk_max(vb, nvis - c * 32 - 32));
+          mraw = fmaxf(mraw, chunk_max(va, ncol(c)));
+          mraw = fmaxf(mraw, chunk_max(vb, ncol(c + 1)));
         }
         const float mt = mraw * sl2;
         const float mn = fmaxf(m_ref, mt);
@@ -731,7 +829,7 @@ __global__ void __launch_bounds__(prefill_detail::kThreads, 1)
           uint32_t va[32];
           ptx::TmemLd<32>::run(sbase + c * 32, va);
           ptx::tmem_wait_ld();
-          write_p(va, sbase + c * 32, nvis - c * 32, neg_m, lsum);
+          write_p(va, sbase + c * 32, ncol(c), neg_m, lsum);
         }
         l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
         ptx::tmem_wait_st();

@@ -114,7 +114,19 @@ def test_random_groups(ops, G, Hkv):
     prefix, members whose length equals the prefix.  With one query head
     and an odd number of sequences the partial-result rows are odd in
     number, which the workspace layout must still keep 16-byte aligned."""
-    bs, D = 16, 128
+    _random_groups(ops, G, Hkv, 16)
+
+
+@pytest.mark.parametrize("bs", [8, 64, 128])
+def test_random_groups_block_sizes(ops, bs):
+    """The same groups at other block sizes: up to 64 the own-token items hold
+    two members each (one block per box in a 64-key half, one box at 64), at
+    128 one member each."""
+    _random_groups(ops, 4, 2, bs)
+
+
+def _random_groups(ops, G, Hkv, bs):
+    D = 128
     H = G * Hkv
     rng = np.random.default_rng(70 + G)
     NB = 900
@@ -122,7 +134,9 @@ def test_random_groups(ops, G, Hkv):
     kc = torch.zeros((NB, Hkv, bs, D), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
     mirror = _Mirror(tuple(kc.shape))
-    spec = [(5, 480), (1, 0), (3, 32), (40, 160), (1, 0), (2, 1024), (3, 0)]  # (members, prefix tokens)
+    # (members, prefix tokens), the prompts cut to whole blocks (members then
+    # append past an unshared block)
+    spec = [(m, P // bs * bs) for m, P in [(5, 480), (1, 0), (3, 32), (40, 160), (1, 0), (2, 1024), (3, 0)]]
     seqs, groups = [], []
     for members, P in spec:
         root = ga.seq_create()
@@ -144,13 +158,14 @@ def test_random_groups(ops, G, Hkv):
             seqs.append(s)
         ga.free_seq(root)
         groups.append(g)
-    tables, lens = ga.export_tables(seqs, 80)
+    tables, lens = ga.export_tables(seqs, -(-1100 // bs) + 2)
     qv = W.Values.from_f32(rng.standard_normal((len(seqs), H, D)).astype(np.float32), "bf16")
     q = to_device(qv)
     scale = float(np.float32(1 / np.sqrt(D)))
     out, st, prefix = _shared_decode(ops, q, kc, vc, tables, lens, scale, Hkv, groups, bs)
     assert st == 0
-    # a one-member group may use all its whole blocks as its "prefix"
+    # the members share the prompt's whole blocks; a one-member group may use
+    # all its whole blocks as its "prefix"
     assert [pf for pf, (m, _) in zip(prefix, spec) if m > 1] == [P for m, P in spec if m > 1]
     ref = oracle.paged_decode(qv.f32, mirror.k, mirror.v, tables, lens, scale, Hkv)
     assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
