@@ -74,6 +74,21 @@ def test_prefill_matches_oracle(ops, G, bs):
     assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("G", [1, 4])
+@pytest.mark.parametrize("bs", [64, 128, 256])
+def test_prefill_large_blocks(ops, G, bs):
+    """Blocks of 64 to 256 tokens: one TMA box per block up to 128 rows, two
+    boxes of 128 rows for a 256-token block; bf16 and fp32 output."""
+    c = _case(G, bs, CHUNKS, seed=500 + 10 * G + bs)
+    out, ref, st = _run(ops, c)
+    assert st == 0
+    assert float(np.abs(to_f64(out) - ref).max()) <= TOL["bf16"]
+    out_b, ref_b, st = _run(ops, c, out_dtype=torch.bfloat16)
+    assert st == 0
+    from paged_case import bf16_half_ulp
+    assert (np.abs(to_f64(out_b) - ref_b) <= np.maximum(TOL["bf16"], TOL["bf16"] + bf16_half_ulp(ref_b))).all()
+
+
 def test_prefill_bf16_output_and_long_prompt(ops):
     c = _case(4, 16, [(0, 1000), (1000, 77)], seed=7)
     out, ref, st = _run(ops, c, out_dtype=torch.bfloat16)
