@@ -651,6 +651,51 @@ def prefill_profile(args):
                       "us": round(us, 2), "TFLOP/s": round(flops / (us * 1e-6) / 1e12, 1)}), flush=True)
 
 
+def cuda_core_profile(args):
+    """The CUDA-core decode kernel (fp32 K/V) on the batch-256 workload's
+    lengths, tables and pool: --warmup + --steps back-to-back launches of
+    pa_decode, values drawn on the device."""
+    import torch
+    dev = torch.device("cuda", 0)
+    from paged_kv_cache_142_gb300 import build as B_
+    B_.build(quiet=True)
+    from paged_kv_cache_142_gb300 import ops
+    g = torch.Generator(device=dev).manual_seed(9)
+    wl = W.gqa_bf16(num_seqs=args.num_seqs, block_size=args.block_size, values=False)
+    B, H, Hkv, D, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    a = ops.BlockAllocator(wl.num_blocks, bs, wl.free_order)
+    seqs = [a.seq_create() for _ in range(B)]
+    for s_, n in zip(seqs, wl.context_lens):
+        a.append_tokens(s_, int(n))
+    tb, ln = a.export_tables(seqs, wl.max_blocks_per_seq)
+    a.close()
+    kc = torch.randn((wl.num_blocks, Hkv, bs, D), generator=g, device=dev) * wl.sigma
+    vc = torch.randn((wl.num_blocks, Hkv, bs, D), generator=g, device=dev) * wl.sigma
+    q = torch.randn((B, H, D), generator=g, device=dev) * wl.sigma
+    out = torch.empty_like(q)
+    ml = int(ln.max())
+    ws = ops.make_workspace(B, H, Hkv, D, bs, "f32", ml, args.partition_tokens, device=dev)
+    d_tb, d_ln = torch.from_numpy(tb).to(dev), torch.from_numpy(ln).to(dev)
+    run = lambda: ops.pa_decode(out, q, kc, vc, d_tb, d_ln, wl.scale, Hkv, ml, ws,
+                                partition_tokens=args.partition_tokens)
+    for _ in range(args.warmup):
+        run()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        run()
+    t1.record()
+    torch.cuda.synchronize()
+    if ops.pa_workspace_error(ws) != 0:
+        raise RuntimeError("pa_decode reported an error")
+    us = t0.elapsed_time(t1) * 1000.0 / args.steps
+    by = int(ln.sum()) * Hkv * D * 4 * 2 + 2 * B * H * D * 4
+    pt, ctas = ops.pa_decode_plan(B, H, Hkv, D, bs, "f32", ml, args.partition_tokens)
+    print(json.dumps({"profile_cuda_core": True, "num_seqs": B, "dtype": "f32", "us": round(us, 2),
+                      "bytes": by, "GB/s": round(by / (us * 1e-6) / 1e9, 1),
+                      "partition_tokens": pt, "ctas": ctas}), flush=True)
+
+
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
@@ -1004,6 +1049,9 @@ def main():
     ap.add_argument("--profile-kernels", action="store_true",
                     help="profiling case: --warmup + --steps launches of each secondary kernel "
                          "(append, copy, shared-prefix decode, prefill) at its bench size")
+    ap.add_argument("--profile-cuda-core", action="store_true",
+                    help="profiling case: only the CUDA-core decode kernel (fp32 K/V) on the batch's "
+                         "lengths, --warmup + --steps back-to-back launches")
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="PROMPTS",
                     help="profiling case: only pa_prefill on PROMPTS causal prompts of 2048 tokens "
                          "(32 q / 8 kv heads), --warmup + --steps launches")
@@ -1012,6 +1060,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.profile_kernels:
         kernel_profile(args)
+    elif args.profile_cuda_core:
+        cuda_core_profile(args)
     elif args.profile_prefill:
         prefill_profile(args)
     elif args.impl == "reference":
